@@ -1,0 +1,246 @@
+/*
+ * mpk.h -- C ABI of the GB300 (sm_103a) mega-kernel decode runtime.
+ *
+ * One LLM decode step is compiled into a task/event graph (tGraph) and run
+ * inside one persistent kernel: "MPK: A Compiler and Runtime for
+ * Mega-Kernelizing Tensor Programs" (§2 Q2, §4, Table 1).  Two calls carry
+ * the method: mpk_build_tgraph (model shape + tile sizes -> tGraph) and
+ * mpk_decode_step (graph + tokens + paged KV cache + stream -> one step).
+ *
+ * Conventions for every call:
+ *   - All tensors are row-major.  bf16 tensors are IEEE bfloat16 bit
+ *     patterns (uint16).  Pointers named d_* and every pointer inside
+ *     mpk_weights / mpk_kv_cache are CUDA device pointers on the device that
+ *     is current when mpk_bind_weights is called; all other pointers are host
+ *     pointers.
+ *   - Ownership: the caller owns weights, KV pools, page tables, seq_lens,
+ *     tokens, logits and next-token buffers, and keeps them alive while the
+ *     graph uses them (pointers are borrowed, never copied or freed).  The
+ *     library owns the graph, its device encoding (descriptors, queues,
+ *     counters) and the activation workspace, all released by
+ *     mpk_destroy_tgraph.
+ *   - Errors: host-detectable errors are returned synchronously and leave
+ *     the graph unchanged.  Errors detected inside the kernel (a bounded wait
+ *     that ran out, an unmapped KV page, a full queue) are latched in a
+ *     device status word that mpk_get_status reads; the kernel then exits
+ *     cleanly and the graph needs mpk_reset before the next step.
+ *   - Threading: no global state.  One graph is used by one host thread and
+ *     one stream at a time; distinct graphs are independent.
+ */
+#ifndef MPK_H_
+#define MPK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MPK_OK = 0,
+  MPK_ERR_INVALID_ARG = 1,     /* a null pointer, a non-positive size, ... */
+  MPK_ERR_UNSUPPORTED = 2,     /* a shape the task bodies do not handle    */
+  MPK_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed         */
+  MPK_ERR_OOM = 4,             /* device or host allocation failed          */
+  MPK_ERR_NOT_CORESIDENT = 5,  /* workers + schedulers exceed the SMs, or
+                                  the persistent grid cannot be co-resident */
+  MPK_ERR_TIMEOUT = 6,         /* a bounded device wait ran out             */
+  MPK_ERR_KV_PAGE = 7,         /* page_table holds -1 where a token lives   */
+  MPK_ERR_QUEUE_OVERFLOW = 8,  /* a device queue could not take an entry    */
+  MPK_ERR_GRAPH_INVALID = 9,   /* the built graph failed its invariants     */
+  MPK_ERR_NOT_BOUND = 10       /* decode before mpk_bind_weights            */
+} mpk_status;
+
+/* Model shape.  Decoder mode: n_layers >= 1, chain_ffn == 0.  Chained-linear
+ * mode: n_layers == 0 and chain_ffn > 0; the step is then
+ * x = embed[token]; n = RMSNorm(x, final_norm); y = silu(n W1^T);
+ * z = y W2^T; logits = z lm_head^T (no KV cache, no attention). */
+typedef struct {
+  int n_layers;
+  int hidden;
+  int n_q_heads;
+  int n_kv_heads;
+  int head_dim;          /* even, <= 128                                   */
+  int ffn;               /* SwiGLU intermediate size                        */
+  int vocab;
+  float rms_eps;
+  float rope_theta;
+  int qk_norm;           /* 1: per-head RMSNorm of q and k before RoPE      */
+  int chain_ffn;         /* > 0 selects the chained-linear mode             */
+  int page_size;         /* KV tokens per page                              */
+  int max_pages_per_seq; /* columns of the page table                       */
+} mpk_model_shape;
+
+/* Tile sizes and runtime geometry; 0 selects the default. */
+typedef struct {
+  int num_workers;        /* W worker SMs.  0: the SM count of the current
+                             device minus num_sched_sms (needs a GPU)       */
+  int gemv_rows_per_task; /* MatMul output rows per task.  0: each MatMul is
+                             split into min(W, ceil(N/8)) tiles of multiples
+                             of 8 rows                                      */
+  int attn_chunks;        /* split-KV chunks per (sequence, KV head).  0:
+                             max(1, min(ceil(max_ctx/128),
+                             ceil(4W/(batch*n_kv_heads))))                  */
+  int num_sched_sms;      /* SMs running scheduler warps. 0: 4 (Table 1)    */
+  int sched_warps_per_sm; /* 0: 4 (Table 1)                                 */
+  int smem_pages;         /* 32 KB shared-memory pages per worker. 0: 6     */
+} mpk_tile_sizes;
+
+/* Task kinds (one per operator of the decode step). */
+enum {
+  MPK_TASK_EMPTY = 0,     /* normalisation glue: waits, then triggers      */
+  MPK_TASK_NORM1 = 1,     /* residual add + RMSNorm (layer 0: embedding)   */
+  MPK_TASK_QKV = 2,       /* MatMul tile of W_qkv                           */
+  MPK_TASK_ROPE = 3,      /* q/k RMSNorm (optional) + RoPE + KV append      */
+  MPK_TASK_ATTN = 4,      /* paged attention over one KV chunk (JIT)        */
+  MPK_TASK_MERGE = 5,     /* log-sum-exp merge of the chunks (JIT)          */
+  MPK_TASK_O = 6,         /* MatMul tile of W_o                             */
+  MPK_TASK_NORM2 = 7,     /* residual add + RMSNorm                         */
+  MPK_TASK_GATEUP = 8,    /* MatMul tile of W_gate and W_up + SwiGLU        */
+  MPK_TASK_DOWN = 9,      /* MatMul tile of W_down                          */
+  MPK_TASK_FINAL_NORM = 10,
+  MPK_TASK_LM_HEAD = 11,  /* MatMul tile of lm_head, fp32 out + tile argmax */
+  MPK_TASK_ARGMAX = 12,   /* argmax over tile maxima; seq_lens += 1         */
+  MPK_TASK_CHAIN_NORM = 13,
+  MPK_TASK_CHAIN_UP = 14, /* MatMul tile of W1 + SiLU                       */
+  MPK_TASK_CHAIN_DOWN = 15,
+  MPK_TASK_NKINDS = 16
+};
+
+/* Launch classes (hybrid JIT/AOT, MPK summary §2 Q2 and "Design space"). */
+enum {
+  MPK_LAUNCH_AOT = 0,     /* statically placed on one worker's queue        */
+  MPK_LAUNCH_JIT = 1,     /* placed by a scheduler warp when its event fires*/
+  MPK_LAUNCH_INLINE = 2   /* empty task, run by whoever fires its event     */
+};
+
+/* Execution modes of mpk_decode_step. */
+enum {
+  MPK_MODE_MEGAKERNEL = 0,  /* one persistent launch per step (default)     */
+  MPK_MODE_KPO = 1,         /* one launch per operator, same task bodies    */
+  MPK_MODE_KPO_GRAPH = 2    /* the KPO launches replayed from a CUDA Graph  */
+};
+
+/* Per-layer weight tensors, in the order of mpk_weights.layers. */
+enum {
+  MPK_W_LN1 = 0,     /* bf16 [hidden]                                       */
+  MPK_W_QKV = 1,     /* bf16 [(Hq + 2 Hkv) d][hidden]: q heads, k heads, v  */
+  MPK_W_QNORM = 2,   /* bf16 [d] (qk_norm only, else ignored)               */
+  MPK_W_KNORM = 3,   /* bf16 [d] (qk_norm only, else ignored)               */
+  MPK_W_O = 4,       /* bf16 [hidden][Hq d]                                 */
+  MPK_W_LN2 = 5,     /* bf16 [hidden]                                       */
+  MPK_W_GATEUP = 6,  /* bf16 [2 ffn][hidden]: rows [0,ffn) gate, then up    */
+  MPK_W_DOWN = 7,    /* bf16 [hidden][ffn]                                  */
+  MPK_LAYER_NTENSORS = 8
+};
+
+typedef struct mpk_graph mpk_graph; /* opaque, library-owned */
+
+/* Device weight pointers (borrowed).  Every bf16 tensor must be 16-byte
+ * aligned.  `layers` is a HOST array of n_layers * MPK_LAYER_NTENSORS device
+ * pointers, read during the call only. */
+typedef struct {
+  const void* embed;           /* bf16 [vocab][hidden]                       */
+  const void* final_norm;      /* bf16 [hidden]                              */
+  const void* lm_head;         /* bf16 [vocab][hidden]                       */
+  const void* const* layers;   /* decoder mode                               */
+  const void* chain_w1;        /* chained mode: bf16 [chain_ffn][hidden]     */
+  const void* chain_w2;        /* chained mode: bf16 [hidden][chain_ffn]     */
+} mpk_weights;
+
+/* Paged KV cache (caller-owned device memory).  Token t of sequence b lives
+ * in page page_table[b][t / page_size] at slot t % page_size. */
+typedef struct {
+  void* k_pool;                /* bf16 [n_layers][num_pages][Hkv][page_size][d] */
+  void* v_pool;                /* same layout                                */
+  const int32_t* page_table;   /* int32 [batch][max_pages_per_seq], -1 = none */
+  int32_t* seq_lens;           /* int32 [batch]: tokens already cached       */
+  int num_pages;
+} mpk_kv_cache;
+
+/* Host arrays describing a built graph, owned by the graph (valid until
+ * mpk_destroy_tgraph).  Tasks and events are in linearised order. */
+typedef struct {
+  int n_tasks, n_events, n_ops, n_empty, n_workers, attn_chunks;
+  const int32_t* task_kind;    /* MPK_TASK_*                                 */
+  const int32_t* task_op;      /* operator index, -1 for empty tasks         */
+  const int32_t* task_layer;   /* layer (n_layers for the final operators)   */
+  const int32_t* task_tile;    /* tile index within its operator             */
+  const int32_t* task_row0;    /* MatMul: output rows [row0, row1)           */
+  const int32_t* task_row1;
+  const int32_t* task_b;       /* attention family: sequence, KV head, chunk */
+  const int32_t* task_g;
+  const int32_t* task_c;
+  const int32_t* task_dep;     /* the one event the task waits on            */
+  const int32_t* task_trig;    /* the one event the task triggers            */
+  const int32_t* task_launch;  /* MPK_LAUNCH_*                               */
+  const int32_t* task_worker;  /* AOT worker, -1 otherwise                   */
+  const int32_t* task_pre_id;  /* id before linearisation (program order)    */
+  const int32_t* event_count;  /* triggers needed to activate the event      */
+  const int32_t* event_first;  /* dependent tasks are [first, last]          */
+  const int32_t* event_last;
+  const int32_t* op_kind;      /* per operator, in program order             */
+  const int32_t* op_layer;
+  const int32_t* op_n_tasks;
+  int64_t n_raw_events;        /* events before fusion                       */
+  int64_t n_fused_events;      /* events after fusion, before normalisation  */
+} mpk_graph_export;
+
+/* Decompose one decode step of `shape` at `batch` sequences into per-tile
+ * tasks, derive events from overlapping output/input regions, fuse them
+ * (Defs 4.1 and 4.2), normalise (<= 1 dependent and <= 1 triggering event
+ * per task) and BFS-linearise (each event's fan-out is [first, last]).
+ * MPK summary §2 Q2 and §4 "6 minimum checks".  Host only: touches no GPU
+ * unless tiles->num_workers == 0.  On success *out owns a new graph. */
+mpk_status mpk_build_tgraph(const mpk_model_shape* shape,
+                            const mpk_tile_sizes* tiles, int batch,
+                            mpk_graph** out);
+
+/* Copy the graph's device encoding to the current device, allocate the
+ * activation workspace and bind the weights (pointers borrowed).  May be
+ * called again to rebind other weights of the same shape. */
+mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w);
+
+/* Enqueue one decode step on `cuda_stream` (a cudaStream_t, 0 = legacy
+ * default stream): d_tokens int32 [batch] in; d_logits fp32 [batch][vocab]
+ * and d_next_tokens int32 [batch] (greedy, lowest index on ties) out.  Reads
+ * kv->seq_lens[b] as the position of the new token, writes its K/V there,
+ * and on success increments seq_lens in the kernel.  Asynchronous: returns
+ * after the launch(es) are enqueued.  In megakernel mode this is one
+ * cooperative launch of a persistent grid (MPK summary, Figure 1: "a
+ * single launch").  d_tokens may alias the previous step's d_next_tokens. */
+mpk_status mpk_decode_step(mpk_graph* g, const int32_t* d_tokens,
+                           const mpk_kv_cache* kv, float* d_logits,
+                           int32_t* d_next_tokens, void* cuda_stream);
+
+/* Read the device status word of the last step.  Synchronises the device.
+ * MPK_OK, or the first error the kernel latched. */
+mpk_status mpk_get_status(mpk_graph* g);
+
+/* Select MPK_MODE_MEGAKERNEL, MPK_MODE_KPO or MPK_MODE_KPO_GRAPH. */
+mpk_status mpk_set_mode(mpk_graph* g, int mode);
+
+/* Fill *out with host arrays of the built graph (for parity checks). */
+mpk_status mpk_export_tgraph(const mpk_graph* g, mpk_graph_export* out);
+
+/* Clear the device status, abort flag, event counters and queues after an
+ * error (synchronises the device).  The KV cache is the caller's to fix. */
+mpk_status mpk_reset(mpk_graph* g);
+
+/* Free everything the graph owns.  Null is ignored. */
+void mpk_destroy_tgraph(mpk_graph* g);
+
+const char* mpk_status_string(mpk_status s);
+
+/* Test hooks.  mpk_debug_set_wait_timeout_ms bounds every device wait of
+ * later steps (default 2000 ms).  mpk_debug_add_event_count adds `delta` to
+ * the trigger count of linearised event `event` in the device encoding, so a
+ * test can make a wait that never completes and check MPK_ERR_TIMEOUT. */
+mpk_status mpk_debug_set_wait_timeout_ms(mpk_graph* g, int ms);
+mpk_status mpk_debug_add_event_count(mpk_graph* g, int event, int delta);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MPK_H_ */

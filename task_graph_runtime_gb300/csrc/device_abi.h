@@ -1,0 +1,130 @@
+// Plain-old-data structures shared by the host encoder and the sm_103a
+// kernels: the compact device encoding of a linearised tGraph (fixed-size
+// task descriptors, events as {count, first, last}) and the launch
+// parameters.  MPK: A Compiler and Runtime for Mega-Kernelizing Tensor
+// Programs, §2 Q2 ("compact device-memory structure") and "关键实现细节" 2
+// (fixed-size task descriptors).
+#pragma once
+
+#include <stdint.h>
+
+namespace mpk {
+
+// 32-byte task descriptor, in linear order.
+struct TaskDesc {
+  int16_t kind;     // MPK_TASK_*
+  uint8_t launch;   // MPK_LAUNCH_*
+  uint8_t flags;
+  int16_t layer;
+  int16_t b;        // attention family: sequence
+  int32_t dep;      // the one event this task waits on
+  int32_t trig;     // the one event this task triggers
+  int32_t row0;     // MatMul: output rows [row0, row1)
+  int32_t row1;
+  int16_t g;        // KV head
+  int16_t c;        // KV chunk
+  int32_t tile;     // tile index within the operator
+};
+static_assert(sizeof(TaskDesc) == 32, "task descriptor must stay 32 bytes");
+
+enum : uint32_t { EV_HAS_JIT = 1u, EV_HAS_INLINE = 2u };
+
+// 16-byte event descriptor: activated when its counter reaches
+// epoch * count; its dependent tasks are [first, last].
+struct EventDesc {
+  uint32_t count;
+  int32_t first;
+  int32_t last;
+  uint32_t flags;   // EV_HAS_*
+};
+static_assert(sizeof(EventDesc) == 16, "event descriptor must stay 16 bytes");
+
+// Multi-producer single-consumer ring in global memory.  Slot value:
+// (ticket << 32) | payload, ticket = position + 1.  Head and tail live on
+// separate 128-byte lines.
+struct RingHdr {
+  uint32_t tail;
+  uint32_t pad0[31];
+  uint32_t head;
+  uint32_t pad1[31];
+};
+
+// Shape and geometry the kernels need.
+struct Dims {
+  int L, h, Hq, Hkv, d, F, V, chain_ffn, qk_norm;
+  float eps;
+  int B;            // batch
+  int C;            // split-KV chunks per (sequence, KV head)
+  int page_size, max_pages;
+  int n_lm_tiles;
+  int max_ctx;      // rows of the RoPE table
+};
+
+// Activation workspace: one block per layer (identical layout), plus a
+// block of step-global tensors.  Offsets in bytes.
+struct ActLayout {
+  char* base;
+  int64_t layer_stride;
+  int64_t o_h, o_n1, o_qkv, o_q, o_opart, o_attn, o_o, o_hmid, o_n2, o_act,
+      o_dout;
+  int64_t g_nf, g_z, g_amax;   // offsets from the global block
+  int64_t global_block;        // offset of the global block from base
+};
+
+struct DevGraph {
+  const TaskDesc* tasks;
+  const EventDesc* events;
+  int n_tasks, n_events;
+  int root, end;
+  const int32_t* aot_list;     // per worker, linear task ids in order
+  const int32_t* aot_off;      // [W + 1]
+  const int32_t* op_tasks;     // per operator, linear ids in tile order
+  uint32_t* counters;          // [n_events]
+  RingHdr* jit_hdr;            // [W]
+  uint64_t* jit_slots;         // [W][jit_cap]
+  RingHdr* sched_hdr;          // [S]
+  uint64_t* sched_slots;       // [S][sched_cap]
+  uint32_t jit_cap, sched_cap;
+  uint32_t* status;            // latched mpk_status
+  uint32_t* abort_flag;
+  int W;                       // worker CTAs
+  int S;                       // scheduler warps in total
+  int sched_warps_per_sm;
+  int n_pages;                 // shared-memory pages per worker
+};
+
+struct WeightPtrs {
+  const uint16_t* embed;
+  const uint16_t* final_norm;
+  const uint16_t* lm_head;
+  const uint16_t* const* layers;   // device array [L][MPK_LAYER_NTENSORS]
+  const uint8_t* tmaps;            // device array of 128-byte tensor maps
+  const float* rope_cs;            // [max_ctx][d/2][2] (cos, sin)
+};
+
+// Tensor-map slots: layer l uses 4l + {0 qkv, 1 o, 2 gate-up, 3 down};
+// then lm_head, chain W1, chain W2.
+enum { TM_QKV = 0, TM_O = 1, TM_GU = 2, TM_DOWN = 3 };
+
+struct StepArgs {
+  const int32_t* tokens;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  const int32_t* page_table;
+  int32_t* seq_lens;
+  int num_pages;
+  float* logits;
+  int32_t* next_tokens;
+  uint32_t epoch;               // step number since the last reset, >= 1
+  uint64_t timeout_ns;
+};
+
+struct KernelParams {
+  Dims dims;
+  DevGraph graph;
+  WeightPtrs w;
+  ActLayout act;
+  StepArgs step;
+};
+
+}  // namespace mpk
