@@ -85,6 +85,18 @@ def residual_add(a: np.ndarray, b: np.ndarray) -> np.ndarray:
 
 
 # ------------------------------------------------------------------- linear
+# Accumulator of every MatMul: float32 (the pages' contract) by default.
+# ``set_accumulator(np.float64)`` selects an exact-in-practice accumulator;
+# the two variants differ only in rounding order and are used to measure the
+# rounding-order noise of the whole bf16 pipeline.
+_ACC = np.float32
+
+
+def set_accumulator(dtype) -> None:
+    global _ACC
+    _ACC = np.dtype(dtype).type
+
+
 def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
     """y = x . W^T with bf16 operands and an FP32 accumulator (MPK summary,
     §3: MatMul task, "bf16 input/output, FP32 accumulator").  x: [B, K] bf16
@@ -93,6 +105,9 @@ def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
     boundary."""
     xf = bf16_to_f32(x)
     wf = bf16_to_f32(w)
+    if _ACC is not F32:
+        xf = xf.astype(_ACC)
+        wf = wf.astype(_ACC)
     return np.matmul(xf, wf.T).astype(F32)
 
 

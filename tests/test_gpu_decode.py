@@ -218,14 +218,6 @@ def test_unmapped_kv_page_is_reported(tiny):
 
 
 # ----------------------------------------------------- configured sizes
-def test_llama1b_two_steps():
-    wl = synth.WORKLOADS["llama1b"]
-    W, kv, tok = _inputs(wl)
-    gpu, _ = run_gpu(wl, dev_weights(W, wl.shape), kv, tok, steps=2)
-    ref, _ = run_oracle(wl, W, kv, tok, steps=2)
-    check_steps(gpu, ref)
-
-
 @pytest.mark.parametrize("name", ["chain_b1", "chain_b8"])
 def test_chain_full_size(name):
     wl = synth.WORKLOADS[name]

@@ -321,3 +321,18 @@ def test_chain_step_matches_torch_float64():
     y = Fn.silu(Fn.linear(x, T(W["chain_w1"])))
     ref = Fn.linear(Fn.linear(y, T(W["chain_w2"])), T(W["lm_head"])).numpy()
     assert np.abs(out["logits"] - ref).max() <= 2e-2 * np.abs(ref).max() + 1e-3
+
+
+def test_float64_accumulator_is_closer_to_exact():
+    """The float64 accumulator variant agrees with torch float64 to fp64
+    rounding, and the default (float32) stays within its gamma_K bound."""
+    K = 4096
+    x = rand_bf16((2, K))
+    W = rand_bf16((16, K), 0.02)
+    ref = Fn.linear(bits_to_torch64(x), bits_to_torch64(W)).numpy()
+    try:
+        nx.set_accumulator(np.float64)
+        y64 = nx.linear(x, W).astype(np.float64)
+    finally:
+        nx.set_accumulator(np.float32)
+    assert np.all(np.abs(y64 - ref) <= 2**-24 * np.abs(ref) + 1e-30)
