@@ -240,6 +240,17 @@ const char* mpk_status_string(mpk_status s);
 mpk_status mpk_debug_set_wait_timeout_ms(mpk_graph* g, int ms);
 mpk_status mpk_debug_add_event_count(mpk_graph* g, int event, int delta);
 
+/* Tracing (megakernel mode).  mpk_debug_set_trace(g, capacity) allocates
+ * room for `capacity` task records (0 disables).  Each executed task adds one
+ * record of four uint64: task id | (worker << 32), and the %globaltimer
+ * nanoseconds at which the worker's leader started looking for it, found it
+ * ready and finished it (after its trigger).  mpk_debug_read_trace copies up
+ * to `capacity` records into host_records, stores the count, and clears the
+ * trace for the next steps (synchronises the device). */
+mpk_status mpk_debug_set_trace(mpk_graph* g, int capacity);
+mpk_status mpk_debug_read_trace(mpk_graph* g, uint64_t* host_records,
+                                int capacity, int* n_records);
+
 #ifdef __cplusplus
 }
 #endif

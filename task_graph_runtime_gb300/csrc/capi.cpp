@@ -12,80 +12,14 @@
 #include <vector>
 
 #include "device_abi.h"
+#include "graph_state.h"
 #include "launch.h"
 #include "mpk.h"
 #include "tgraph_builder.h"
 
 using namespace mpk;
 
-namespace {
-
-constexpr uint32_t kJitCap = 1024;
-constexpr uint32_t kSchedCap = 4096;
-constexpr int kDefaultPages = 6;
-constexpr int kSmemLimit = 232448;   // 227 KB per block on sm_100-class
-
-template <typename T>
-struct DevBuf {
-  T* p = nullptr;
-  size_t n = 0;
-  ~DevBuf() { reset(); }
-  void reset() {
-    if (p) cudaFree(p);
-    p = nullptr;
-    n = 0;
-  }
-  cudaError_t alloc(size_t count) {
-    reset();
-    n = count;
-    if (count == 0) return cudaSuccess;
-    return cudaMalloc(reinterpret_cast<void**>(&p), count * sizeof(T));
-  }
-  cudaError_t upload(const std::vector<T>& v) {
-    cudaError_t e = alloc(v.size());
-    if (e != cudaSuccess || v.empty()) return e;
-    return cudaMemcpy(p, v.data(), v.size() * sizeof(T),
-                      cudaMemcpyHostToDevice);
-  }
-};
-
-}  // namespace
-
-struct mpk_graph {
-  BuiltGraph bg;
-  int num_sched_sms = 4, sched_warps_per_sm = 4, pages_req = kDefaultPages;
-  // export arrays (linear order)
-  std::vector<int32_t> x_kind, x_op, x_layer, x_tile, x_row0, x_row1, x_b,
-      x_g, x_c, x_pre, op_kind, op_layer, op_n;
-  // device encoding
-  int device = -1;
-  bool encoded = false, bound = false;
-  std::vector<TaskDesc> h_tasks;
-  std::vector<EventDesc> h_events;
-  std::vector<int32_t> h_aot, h_aot_off, h_op_tasks, h_op_first;
-  DevBuf<TaskDesc> d_tasks;
-  DevBuf<EventDesc> d_events;
-  DevBuf<int32_t> d_aot, d_aot_off, d_op_tasks;
-  DevBuf<uint32_t> d_counters, d_status;
-  DevBuf<RingHdr> d_jit_hdr, d_sched_hdr;
-  DevBuf<uint64_t> d_jit_slots, d_sched_slots;
-  DevBuf<char> d_act;
-  DevBuf<uint8_t> d_tmaps;
-  DevBuf<const uint16_t*> d_layer_ptrs;
-  DevBuf<float> d_rope;
-  KernelParams params{};
-  int smem = 0, n_pages = 0;
-  uint32_t epoch = 0;
-  uint64_t timeout_ns = 2000000000ull;
-  int mode = MPK_MODE_MEGAKERNEL;
-  // captured kernel-per-operator step
-  cudaGraphExec_t kpo_exec = nullptr;
-  StepArgs kpo_args{};
-  cudaStream_t kpo_stream = nullptr;
-  ~mpk_graph() {
-    if (kpo_exec) cudaGraphExecDestroy(kpo_exec);
-  }
-};
+using namespace mpk_detail;
 
 namespace {
 
@@ -646,6 +580,42 @@ mpk_status mpk_debug_add_event_count(mpk_graph* g, int event, int delta) {
     CK(cudaMemcpy(g->d_events.p + event, &g->h_events[event],
                   sizeof(EventDesc), cudaMemcpyHostToDevice));
   }
+  return MPK_OK;
+}
+
+mpk_status mpk_debug_set_trace(mpk_graph* g, int capacity) {
+  if (!g || capacity < 0) return MPK_ERR_INVALID_ARG;
+  if (!g->bound) return MPK_ERR_NOT_BOUND;
+  CK(cudaDeviceSynchronize());
+  g->d_trace.reset();
+  g->d_trace_count.reset();
+  g->params.graph.trace = nullptr;
+  g->params.graph.trace_count = nullptr;
+  g->params.graph.trace_cap = 0;
+  if (capacity == 0) return MPK_OK;
+  CK(g->d_trace.alloc((size_t)capacity * 4));
+  CK(g->d_trace_count.alloc(1));
+  CK(cudaMemset(g->d_trace_count.p, 0, sizeof(uint32_t)));
+  g->params.graph.trace = g->d_trace.p;
+  g->params.graph.trace_count = g->d_trace_count.p;
+  g->params.graph.trace_cap = (uint32_t)capacity;
+  return MPK_OK;
+}
+
+mpk_status mpk_debug_read_trace(mpk_graph* g, uint64_t* host_records,
+                                int capacity, int* n_records) {
+  if (!g || !n_records || capacity < 0) return MPK_ERR_INVALID_ARG;
+  if (!g->d_trace.p) return MPK_ERR_INVALID_ARG;
+  CK(cudaDeviceSynchronize());
+  uint32_t n = 0;
+  CK(cudaMemcpy(&n, g->d_trace_count.p, sizeof(n), cudaMemcpyDeviceToHost));
+  if (n > g->params.graph.trace_cap) n = g->params.graph.trace_cap;
+  const int take = (int)n < capacity ? (int)n : capacity;
+  if (take > 0 && host_records)
+    CK(cudaMemcpy(host_records, g->d_trace.p, (size_t)take * 32,
+                  cudaMemcpyDeviceToHost));
+  CK(cudaMemset(g->d_trace_count.p, 0, sizeof(uint32_t)));
+  *n_records = take;
   return MPK_OK;
 }
 

@@ -87,6 +87,9 @@ struct DevGraph {
   uint32_t jit_cap, sched_cap;
   uint32_t* status;            // latched mpk_status
   uint32_t* abort_flag;
+  uint64_t* trace;             // nullable: 4 words per executed task
+  uint32_t* trace_count;
+  uint32_t trace_cap;          // records
   int W;                       // worker CTAs
   int S;                       // scheduler warps in total
   int sched_warps_per_sm;

@@ -1197,8 +1197,10 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
   if (tid == 0) jit_head = ld_relaxed(&jh->head);
   Ring ring{0, 0};
   int iter = 0;
+  uint64_t t_look = 0, t_ready = 0;
   while (true) {
     if (tid == 0) {
+      if (G.trace) t_look = globaltimer();
       int cmd = -1;
       uint32_t spins = 0;
       int head_task = (ai < a1) ? G.aot_list[ai] : -1;
@@ -1225,6 +1227,7 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
         }
       }
       fence_acq_rel_gpu();
+      if (G.trace) t_ready = globaltimer();
       S.ctrl[iter & 1] = cmd;
     }
     consumer_sync();
@@ -1239,6 +1242,17 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
     if (tid == 0 && !S.ctrl[2] && !aborted(P)) {
       __threadfence();
       trigger(P, t.trig, deadline);
+      if (G.trace) {
+        // (task | worker << 32), looked-for, ready, done
+        const uint32_t k = atomicAdd(G.trace_count, 1u);
+        if (k < G.trace_cap) {
+          uint64_t* r = G.trace + 4ull * k;
+          r[0] = (uint64_t)(uint32_t)cmd | ((uint64_t)(uint32_t)w << 32);
+          r[1] = t_look;
+          r[2] = t_ready;
+          r[3] = globaltimer();
+        }
+      }
     }
   }
 }

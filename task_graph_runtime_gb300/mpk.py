@@ -115,6 +115,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mpk_status_string": ([i], ctypes.c_char_p),
         "mpk_debug_set_wait_timeout_ms": ([vp, i], st),
         "mpk_debug_add_event_count": ([vp, i, i], st),
+        "mpk_debug_set_trace": ([vp, i], st),
+        "mpk_debug_read_trace": ([vp, vp, i, ctypes.POINTER(i)], st),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -283,6 +285,19 @@ class Graph:
                                                         delta),
                "mpk_debug_add_event_count")
 
+    def set_trace(self, capacity: int):
+        _check(load_library().mpk_debug_set_trace(self.handle, capacity),
+               "mpk_debug_set_trace")
+
+    def read_trace(self, capacity: int) -> np.ndarray:
+        """uint64 [n, 4]: task | worker << 32, looked, ready, done (ns)."""
+        buf = np.zeros((capacity, 4), np.uint64)
+        n = ctypes.c_int(0)
+        _check(load_library().mpk_debug_read_trace(
+            self.handle, buf.ctypes.data, capacity, ctypes.byref(n)),
+            "mpk_debug_read_trace")
+        return buf[:n.value]
+
     def close(self):
         if self.handle:
             mpk_destroy_tgraph(self.handle)
@@ -293,3 +308,4 @@ class Graph:
             self.close()
         except Exception:
             pass
+
