@@ -251,6 +251,39 @@ mpk_status mpk_debug_set_trace(mpk_graph* g, int capacity);
 mpk_status mpk_debug_read_trace(mpk_graph* g, uint64_t* host_records,
                                 int capacity, int* n_records);
 
+/* Allocation-free decode step.  (The paper has no counterpart: this is a
+ * convenience for callers of the library.)
+ *
+ * For callers that cannot call cudaMalloc while they run: a serving process
+ * whose device memory is reserved up front by its own caching allocator, a
+ * latency-critical loop that may not take the device-wide synchronisation
+ * cudaMalloc/cudaFree imply, or a plugin whose host owns every allocation.
+ * The call runs the kernel-per-operator form of the step (the same task
+ * bodies as mpk_decode_step) and keeps all of its scratch -- descriptors,
+ * TMA descriptors, the RoPE table, the activation workspace and the status
+ * word -- in one static device array of MPK_NOALLOC_SCRATCH_BYTES that every
+ * GPU loading the library holds until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * g comes from mpk_build_tgraph (mpk_bind_weights is not needed); w, d_tokens,
+ * kv, d_logits and d_next_tokens are as for mpk_bind_weights and
+ * mpk_decode_step, on the current device.  d_status (nullable, device
+ * uint32) receives the step's mpk_status once the step has run.
+ * Returns MPK_ERR_UNSUPPORTED, before touching the device, when the graph
+ * needs more scratch than MPK_NOALLOC_SCRATCH_BYTES (8 MiB: e.g. the tiny,
+ * ~1B-parameter and chained-linear shapes fit, the 36-layer 8B shape does
+ * not).  The first call on a device looks up the array's device address,
+ * so make that first call before any stream capture.  All calls share the
+ * one array, which keeps the last call's contents: calls that overlap on
+ * the GPU (other streams, or other host threads) race and must not be
+ * issued.  Asynchronous on cuda_stream. */
+#define MPK_NOALLOC_SCRATCH_BYTES (8u << 20)
+mpk_status mpk_decode_step_noalloc(const mpk_graph* g, const mpk_weights* w,
+                                   const int32_t* d_tokens,
+                                   const mpk_kv_cache* kv, float* d_logits,
+                                   int32_t* d_next_tokens, uint32_t* d_status,
+                                   void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

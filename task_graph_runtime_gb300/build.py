@@ -46,6 +46,9 @@ def build(verbose: bool = False) -> str:
         [nvcc] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler",
                          "-fPIC", "-c", os.path.join(CSRC, "kernels.cu"),
                          "-o", os.path.join(BUILD_DIR, "kernels.o")] + inc,
+        [nvcc] + ARCH + ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-c",
+                         os.path.join(CSRC, "noalloc.cu"), "-o",
+                         os.path.join(BUILD_DIR, "noalloc.o")] + inc,
         ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-c",
          os.path.join(CSRC, "capi.cpp"), "-o",
          os.path.join(BUILD_DIR, "capi.o")] + inc,
@@ -60,6 +63,7 @@ def build(verbose: bool = False) -> str:
     tmp = OUT + ".tmp"
     _run([nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp,
                           os.path.join(BUILD_DIR, "kernels.o"),
+                          os.path.join(BUILD_DIR, "noalloc.o"),
                           os.path.join(BUILD_DIR, "capi.o"),
                           os.path.join(BUILD_DIR, "tgraph_builder.o"),
                           "-Xlinker", "-rpath=" + os.path.join(cuda, "lib64")])

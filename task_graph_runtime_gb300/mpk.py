@@ -117,6 +117,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mpk_debug_add_event_count": ([vp, i, i], st),
         "mpk_debug_set_trace": ([vp, i], st),
         "mpk_debug_read_trace": ([vp, vp, i, ctypes.POINTER(i)], st),
+        "mpk_decode_step_noalloc": ([vp, ctypes.POINTER(_Weights), vp,
+                                     ctypes.POINTER(_KVCache), vp, vp, vp,
+                                     vp], st),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -309,3 +312,20 @@ class Graph:
         except Exception:
             pass
 
+
+def mpk_decode_step_noalloc(graph: "Graph", weights: Weights, tokens, kv,
+                            logits, next_tokens, status=None, stream=None):
+    """One decode step with every piece of scratch in the library's static
+    device array (no device allocation); see include/mpk.h."""
+    import torch
+    s = (torch.cuda.current_stream().cuda_stream if stream is None
+         else stream if isinstance(stream, int) else stream.cuda_stream)
+    st, layers = weights.c_struct()
+    kvs = kv.c_struct() if kv is not None else None
+    _check(load_library().mpk_decode_step_noalloc(
+        graph.handle, ctypes.byref(st), tokens.data_ptr(),
+        ctypes.byref(kvs) if kvs is not None else None, logits.data_ptr(),
+        next_tokens.data_ptr(),
+        status.data_ptr() if status is not None else None, s),
+        "mpk_decode_step_noalloc")
+    return layers          # keep the host pointer array alive until here
