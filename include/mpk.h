@@ -76,36 +76,47 @@ typedef struct {
 typedef struct {
   int num_workers;        /* W worker SMs.  0: the SM count of the current
                              device minus num_sched_sms (needs a GPU)       */
-  int gemv_rows_per_task; /* MatMul output rows per task.  0: each MatMul is
-                             split into min(W, ceil(N/8)) tiles of multiples
-                             of 8 rows                                      */
+  int gemv_rows_per_task; /* MatMul output rows per task at batch < 8 (a
+                             multiple of 8).  0: T = W * ceil(ceil(N/cap)/W)
+                             tiles (at most ceil(N/8)) of multiples of 8
+                             rows, cap = 2048 page rows at batch 1 and 64 at
+                             batch 2..7 (a gate/up row counts twice)        */
+  int mma_rows_per_task;  /* the same for batch >= 8, where MatMul tiles run
+                             on tensor cores; 0: as above with cap = 128    */
   int attn_chunks;        /* split-KV chunks per (sequence, KV head).  0:
                              max(1, min(ceil(max_ctx/128),
                              ceil(4W/(batch*n_kv_heads))))                  */
   int num_sched_sms;      /* SMs running scheduler warps. 0: 4 (Table 1)    */
   int sched_warps_per_sm; /* 0: 4 (Table 1)                                 */
-  int smem_pages;         /* 32 KB shared-memory pages per worker. 0: 6     */
+  int smem_pages;         /* weight pages (8 rows x 2048 columns, 32 KB +
+                             row skew) per worker. 0: as many as fit, <= 6  */
+  int l2_prefetch_pages;  /* pages each worker prefetches into L2 beyond its
+                             shared-memory ring. 0: 8; < 0: none            */
+  int coarse_events;      /* 1: every task of an operator waits for every
+                             task of the operators it reads (the
+                             operator-level graph of Figure 4c, an
+                             ablation); 0: region-overlap events           */
 } mpk_tile_sizes;
 
 /* Task kinds (one per operator of the decode step). */
 enum {
   MPK_TASK_EMPTY = 0,     /* normalisation glue: waits, then triggers      */
-  MPK_TASK_NORM1 = 1,     /* residual add + RMSNorm (layer 0: embedding)   */
-  MPK_TASK_QKV = 2,       /* MatMul tile of W_qkv                           */
-  MPK_TASK_ROPE = 3,      /* q/k RMSNorm (optional) + RoPE + KV append      */
-  MPK_TASK_ATTN = 4,      /* paged attention over one KV chunk (JIT)        */
-  MPK_TASK_MERGE = 5,     /* log-sum-exp merge of the chunks (JIT)          */
-  MPK_TASK_O = 6,         /* MatMul tile of W_o                             */
-  MPK_TASK_NORM2 = 7,     /* residual add + RMSNorm                         */
-  MPK_TASK_GATEUP = 8,    /* MatMul tile of W_gate and W_up + SwiGLU        */
-  MPK_TASK_DOWN = 9,      /* MatMul tile of W_down                          */
-  MPK_TASK_FINAL_NORM = 10,
-  MPK_TASK_LM_HEAD = 11,  /* MatMul tile of lm_head, fp32 out + tile argmax */
-  MPK_TASK_ARGMAX = 12,   /* argmax over tile maxima; seq_lens += 1         */
-  MPK_TASK_CHAIN_NORM = 13,
-  MPK_TASK_CHAIN_UP = 14, /* MatMul tile of W1 + SiLU                       */
-  MPK_TASK_CHAIN_DOWN = 15,
-  MPK_TASK_NKINDS = 16
+  MPK_TASK_QKV = 1,       /* MatMul tile of W_qkv; prologue: residual add
+                             (layer 0: embedding gather) + RMSNorm          */
+  MPK_TASK_ATTN = 2,      /* one KV chunk of one (sequence, KV head): q/k
+                             RMSNorm (optional) + RoPE + KV append, paged
+                             attention over the chunk, and the log-sum-exp
+                             merge of all chunks by the last to finish     */
+  MPK_TASK_O = 3,         /* MatMul tile of W_o                             */
+  MPK_TASK_GATEUP = 4,    /* MatMul tile of W_gate and W_up; prologue:
+                             residual add + RMSNorm; epilogue: SwiGLU       */
+  MPK_TASK_DOWN = 5,      /* MatMul tile of W_down                          */
+  MPK_TASK_LM_HEAD = 6,   /* MatMul tile of lm_head (prologue: final norm),
+                             fp32 logits + tile argmax                      */
+  MPK_TASK_ARGMAX = 7,    /* argmax over tile maxima; seq_lens += 1         */
+  MPK_TASK_CHAIN_UP = 8,  /* MatMul tile of W1 (prologue: RMSNorm) + SiLU   */
+  MPK_TASK_CHAIN_DOWN = 9,
+  MPK_TASK_NKINDS = 10
 };
 
 /* Launch classes (hybrid JIT/AOT, MPK summary §2 Q2 and "Design space"). */
@@ -250,6 +261,13 @@ mpk_status mpk_debug_add_event_count(mpk_graph* g, int event, int delta);
 mpk_status mpk_debug_set_trace(mpk_graph* g, int capacity);
 mpk_status mpk_debug_read_trace(mpk_graph* g, uint64_t* host_records,
                                 int capacity, int* n_records);
+
+/* Copy the residual stream entering decoder layer `layer` of the last step
+ * (0 <= layer <= n_layers; n_layers is the input of the final RMSNorm) into
+ * host_out, bf16 [batch][hidden] (synchronises the device).  The first
+ * MatMul tile of each layer (and of lm_head) stores it as a by-product of
+ * its RMSNorm prologue.  Decoder mode only. */
+mpk_status mpk_debug_read_hidden(mpk_graph* g, int layer, uint16_t* host_out);
 
 /* Allocation-free decode step.  (The paper has no counterpart: this is a
  * convenience for callers of the library.)

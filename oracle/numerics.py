@@ -8,7 +8,7 @@ outputs with an FP32 accumulator and round-to-nearest-even (MPK summary, §3
 "Target operation, shapes & precision contract").  Every tensor that crosses
 an operator boundary is rounded to bf16; logits stay fp32.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * RMSNorm rounds once, after the multiply by the gain;
   * RoPE is the rotate-half form, pair (i, i + d/2), angle pos * theta^(-2i/d);
     the angle and its cos/sin are evaluated in float64, the rotation in fp32;

@@ -22,7 +22,7 @@ pairwise comparison of two rectangles.  The steps follow MPK summary, §2 Q2 and
   6. hybrid launch -- attention tasks (data-dependent duration) are JIT,
      the rest AOT (MPK summary, §2 Q2 and "Design space": task launch mode).
 
-Readings taken where the pages are silent (listed in the design doc):
+Readings taken where the pages are silent:
   * raw events are numbered in (producer id, consumer id) order; a fused
     event keeps the smallest id of its members; S-pass then P-pass, repeated
     to a fixpoint; fusion is not re-applied after normalisation;
@@ -39,8 +39,17 @@ Readings taken where the pages are silent (listed in the design doc):
   * AOT tasks, in linear order, are dealt round-robin to the W workers;
     JIT tasks are placed at run time; empty tasks run inline when their
     event fires;
-  * split-KV attention: each (sequence, KV head) has C chunk tasks plus one
-    merge task (log-sum-exp), both JIT.
+  * operators of the decode step (a program-level choice the pages leave to
+    the compiler): every RMSNorm, with the residual add before it, is the
+    prologue of the MatMul that consumes it (each MatMul tile normalises its
+    own copy of the input row; tile 0 also stores the residual sum), and the
+    query/key RMSNorm, RoPE and KV append are the prologue of the attention
+    chunk tasks;
+  * split-KV attention: each (sequence, KV head) has C chunk tasks; the
+    chunk that finishes last merges the C partials (log-sum-exp), so every
+    chunk declares a write of the group's attention output.  Chunks are AOT
+    at batch 1 when no chunk can hold more than 128 tokens (equal work,
+    known ahead), JIT otherwise (data-dependent lengths).
 """
 from __future__ import annotations
 
@@ -54,13 +63,16 @@ AOT, JIT, INLINE = 0, 1, 2
 
 GEMV_KINDS = ("qkv", "o", "gateup", "down", "lm_head", "chain_up",
               "chain_down")
+WHOLE = 1 << 30          # a region axis that spans the whole tensor
 
 
 @dataclasses.dataclass
 class Tiles:
     num_workers: int
-    gemv_rows_per_task: int = 0     # 0: default split into <= W tiles
+    gemv_rows_per_task: int = 0     # batch < 8; 0: default split
     attn_chunks: int = 0            # 0: default from the context length
+    mma_rows_per_task: int = 0      # batch >= 8; 0: default split
+    coarse_events: int = 0          # 1: every read spans its whole tensor
 
 
 @dataclasses.dataclass
@@ -87,16 +99,28 @@ class Op:
     n_tasks: int
 
 
-def row_tiles(n_rows: int, tiles: Tiles) -> List[Tuple[int, int]]:
+def tile_row_cap(batch: int, dual: bool) -> int:
+    """Most output rows of one MatMul tile: 2048 weight rows at batch 1, 64
+    at batch 2..7, 128 at batch >= 8; a gate/up tile streams two weight rows
+    per output row."""
+    rows = 2048 if batch == 1 else (64 if batch < 8 else 128)
+    return rows // 2 if dual else rows
+
+
+def row_tiles(n_rows: int, rows_per_task: int, num_workers: int,
+              cap: int) -> List[Tuple[int, int]]:
     """Split n_rows output rows into tiles.  Explicit size R: tiles of R
-    rows, the last one ragged.  Default: T = min(W, ceil(N/8)) tiles whose
-    sizes are multiples of 8 rows (the last clipped at N), unit boundaries at
-    floor(i * U / T)."""
-    if tiles.gemv_rows_per_task > 0:
-        R = tiles.gemv_rows_per_task
+    rows, the last one ragged.  Default: U = ceil(N/8) units of 8 rows,
+    T0 = ceil(U / (cap/8)) tiles at least, rounded up to a multiple of the
+    worker count W and clipped to U; unit boundaries at floor(i * U / T)."""
+    if rows_per_task > 0:
+        R = rows_per_task
         return [(s, min(n_rows, s + R)) for s in range(0, n_rows, R)]
     U = -(-n_rows // 8)
-    T = min(tiles.num_workers, U)
+    cap_u = max(1, cap // 8)
+    T0 = -(-U // cap_u)
+    W = max(1, num_workers)
+    T = max(1, min(U, W * (-(-T0 // W))))
     out = []
     for i in range(T):
         u0 = (i * U) // T
@@ -112,17 +136,29 @@ def default_attn_chunks(batch: int, n_kv_heads: int, max_ctx: int,
     return max(1, min(by_len, by_workers))
 
 
+def attn_is_aot(batch: int, max_ctx: int, chunks: int) -> bool:
+    """Chunks of equal, known size (batch 1) that fit 128 tokens."""
+    return batch == 1 and chunks > 0 and -(-max_ctx // chunks) <= 128
+
+
 def decompose(shape, batch: int, max_ctx: int, tiles: Tiles):
     """Operators in program order -> tasks with read/write regions.
-    A region is (tensor, r0, r1, c0, c1), half-open rectangles over a 2-D
-    view of the tensor; the KV cache of a layer is the tensor ("kv", l)
-    viewed as [batch, kv head]."""
+    A region is (tensor, r0, r1, c0, c1), a half-open rectangle over a 2-D
+    view of the tensor.  With ``tiles.coarse_events`` every read covers its
+    whole tensor, so every task of an operator depends on every task of the
+    operators it reads (the operator-level graph of Figure 4c)."""
     B = batch
     h, d, F, V = shape.hidden, shape.head_dim, shape.ffn, shape.vocab
     Hq, Hkv = shape.n_q_heads, shape.n_kv_heads
     grp = Hq // Hkv if Hkv else 1
+    L = shape.n_layers
     ops: List[Op] = []
     tasks: List[Task] = []
+
+    def rd(tensor, r0, r1, c0, c1):
+        if tiles.coarse_events:
+            return (tensor, 0, WHOLE, 0, WHOLE)
+        return (tensor, r0, r1, c0, c1)
 
     def add_op(kind, layer, specs):
         op = Op(kind, layer, len(tasks), len(specs))
@@ -133,84 +169,61 @@ def decompose(shape, batch: int, max_ctx: int, tiles: Tiles):
         ops.append(op)
         return op
 
-    def gemv(kind, layer, n_rows, src, dst, k_cols, extra_write=None):
+    def gemv(kind, layer, n_rows, srcs, dst, k_cols, dual=False, resid=None,
+             extra_write=None):
+        rpt = tiles.mma_rows_per_task if B >= 8 else tiles.gemv_rows_per_task
         specs = []
-        for i, (r0, r1) in enumerate(row_tiles(n_rows, tiles)):
+        tl = row_tiles(n_rows, rpt, tiles.num_workers, tile_row_cap(B, dual))
+        for i, (r0, r1) in enumerate(tl):
             w = [(dst, 0, B, r0, r1)]
+            if i == 0 and resid is not None:
+                w.append((resid, 0, B, 0, k_cols))
             if extra_write:
                 w.append((extra_write, 0, B, i, i + 1))
             specs.append(dict(row0=r0, row1=r1,
-                              reads=[(src, 0, B, 0, k_cols)], writes=w))
+                              reads=[rd(src, 0, B, 0, k_cols) for src in srcs],
+                              writes=w))
         return add_op(kind, layer, specs)
 
     if shape.is_chain:
-        add_op("chain_norm", 0, [dict(reads=[],
-                                      writes=[(("n", 0), 0, B, 0, h)])])
-        gemv("chain_up", 0, shape.chain_ffn, ("n", 0), ("act", 0), h)
-        gemv("chain_down", 0, h, ("act", 0), ("z", 0), shape.chain_ffn)
-        lm_src = ("z", 0)
+        # the RMSNorm of the embedding row is W1's prologue
+        gemv("chain_up", 0, shape.chain_ffn, [], ("act", 0), h)
+        gemv("chain_down", 0, h, [("act", 0)], ("z", 0), shape.chain_ffn)
+        lm = gemv("lm_head", 0, V, [("z", 0)], ("logits", 0), h,
+                  extra_write=("amax", 0))
         n_chunks = 0
     else:
         C = tiles.attn_chunks or default_attn_chunks(B, Hkv, max_ctx,
                                                      tiles.num_workers)
         n_chunks = C
-        for l in range(shape.n_layers):
-            rd = [] if l == 0 else [(("hmid", l - 1), 0, B, 0, h),
-                                    (("dout", l - 1), 0, B, 0, h)]
-            add_op("norm1", l, [dict(reads=rd, writes=[(("h", l), 0, B, 0, h),
-                                                       (("n1", l), 0, B, 0, h)])])
-            gemv("qkv", l, shape.qkv_rows, ("n1", l), ("qkv", l), h)
+        for l in range(L):
+            srcs = [] if l == 0 else [("hmid", l - 1), ("dout", l - 1)]
+            gemv("qkv", l, shape.qkv_rows, srcs, ("qkv", l), h,
+                 resid=("h", l))
             specs = []
             for b in range(B):
                 for g in range(Hkv):
                     qc = (g * grp * d, (g + 1) * grp * d)
                     kc = (Hq * d + g * d, Hq * d + (g + 1) * d)
                     vc = ((Hq + Hkv) * d + g * d, (Hq + Hkv) * d + (g + 1) * d)
-                    specs.append(dict(
-                        b=b, g=g,
-                        reads=[(("qkv", l), b, b + 1) + qc,
-                               (("qkv", l), b, b + 1) + kc,
-                               (("qkv", l), b, b + 1) + vc],
-                        writes=[(("q", l), b, b + 1) + qc,
-                                (("kv", l), b, b + 1, g, g + 1)]))
-            add_op("rope", l, specs)
-            specs = []
-            for b in range(B):
-                for g in range(Hkv):
-                    qc = (g * grp * d, (g + 1) * grp * d)
                     for c in range(C):
                         specs.append(dict(
                             b=b, g=g, c=c,
-                            reads=[(("q", l), b, b + 1) + qc,
-                                   (("kv", l), b, b + 1, g, g + 1)],
+                            reads=[rd(("qkv", l), b, b + 1, *qc),
+                                   rd(("qkv", l), b, b + 1, *kc),
+                                   rd(("qkv", l), b, b + 1, *vc)],
                             writes=[(("opart", l), b * Hkv + g,
-                                     b * Hkv + g + 1, c, c + 1)]))
+                                     b * Hkv + g + 1, c, c + 1),
+                                    (("attn", l), b, b + 1) + qc]))
             add_op("attn", l, specs)
-            specs = []
-            for b in range(B):
-                for g in range(Hkv):
-                    qc = (g * grp * d, (g + 1) * grp * d)
-                    specs.append(dict(
-                        b=b, g=g,
-                        reads=[(("opart", l), b * Hkv + g, b * Hkv + g + 1,
-                                0, C)],
-                        writes=[(("attn", l), b, b + 1) + qc]))
-            add_op("merge", l, specs)
-            gemv("o", l, h, ("attn", l), ("o", l), Hq * d)
-            add_op("norm2", l, [dict(
-                reads=[(("h", l), 0, B, 0, h), (("o", l), 0, B, 0, h)],
-                writes=[(("hmid", l), 0, B, 0, h), (("n2", l), 0, B, 0, h)])])
-            gemv("gateup", l, F, ("n2", l), ("act", l), h)
-            gemv("down", l, h, ("act", l), ("dout", l), F)
-        L = shape.n_layers
-        add_op("final_norm", L, [dict(
-            reads=[(("hmid", L - 1), 0, B, 0, h), (("dout", L - 1), 0, B, 0, h)],
-            writes=[(("h", L), 0, B, 0, h), (("nf", 0), 0, B, 0, h)])])
-        lm_src = ("nf", 0)
-    lm = gemv("lm_head", shape.n_layers, V, lm_src, ("logits", 0), h,
-              extra_write=("amax", 0))
-    add_op("argmax", shape.n_layers, [dict(
-        reads=[(("amax", 0), 0, B, 0, lm.n_tasks)],
+            gemv("o", l, h, [("attn", l)], ("o", l), Hq * d)
+            gemv("gateup", l, F, [("h", l), ("o", l)], ("act", l), h,
+                 dual=True, resid=("hmid", l))
+            gemv("down", l, h, [("act", l)], ("dout", l), F)
+        lm = gemv("lm_head", L, V, [("hmid", L - 1), ("dout", L - 1)],
+                  ("logits", 0), h, resid=("h", L), extra_write=("amax", 0))
+    add_op("argmax", L, [dict(
+        reads=[rd(("amax", 0), 0, B, 0, lm.n_tasks)],
         writes=[(("next", 0), 0, B, 0, 1)])])
     return ops, tasks, n_chunks
 
@@ -309,17 +322,18 @@ class Graph:
 def build(shape, batch: int, max_ctx: int, tiles: Tiles) -> Graph:
     """Decompose a decoder step and run every pass on it."""
     ops, tasks, C = decompose(shape, batch, max_ctx, tiles)
-    return build_from_tasks(ops, tasks, tiles.num_workers, C)
+    jit = () if attn_is_aot(batch, max_ctx, C) else ("attn",)
+    return build_from_tasks(ops, tasks, tiles.num_workers, C, jit)
 
 
 def build_from_tasks(ops: List[Op], tasks: List[Task], num_workers: int,
-                     n_chunks: int = 0) -> Graph:
+                     n_chunks: int = 0, jit_kinds=("attn",)) -> Graph:
     """Dependencies, fusion, normalisation, linearisation and AOT assignment
     for an already decomposed task list (tasks[i].id == i)."""
     raw = raw_events(tasks)
     fused = fuse(raw)
     kinds = [t.kind for t in tasks]
-    g = normalize_and_linearize(kinds, fused, num_workers)
+    g = normalize_and_linearize(kinds, fused, num_workers, jit_kinds)
     g.ops, g.n_chunks, g.raw, g.fused = ops, n_chunks, raw, fused
     g.tasks = list(tasks) + [
         Task(id=i, op=-1, kind="empty", layer=-1, tile=0)
@@ -329,7 +343,8 @@ def build_from_tasks(ops: List[Op], tasks: List[Task], num_workers: int,
 
 def normalize_and_linearize(kinds: List[str],
                             fused: Dict[int, Tuple[set, set]],
-                            num_workers: int) -> "Graph":
+                            num_workers: int,
+                            jit_kinds=("attn",)) -> "Graph":
     """Normalisation, root/end events, BFS linearisation and AOT assignment
     on fused events {id: (InTasks, OutTasks)} over tasks 0..len(kinds)-1."""
     ev = {i: (set(a), set(b)) for i, (a, b) in fused.items()}
@@ -430,7 +445,7 @@ def normalize_and_linearize(kinds: List[str],
         if kind == "empty":
             launch.append(INLINE)
             worker.append(-1)
-        elif kind in ("attn", "merge"):
+        elif kind in jit_kinds:
             launch.append(JIT)
             worker.append(-1)
         else:

@@ -1,6 +1,6 @@
 """Compile ``libmpk.so`` in-tree for sm_103a (nvcc + g++, no cmake).
 
-The three translation units compile in parallel; the shared library lands
+The translation units compile in parallel; the shared library lands
 next to this file.  ``python -m task_graph_runtime_gb300.build`` runs it."""
 from __future__ import annotations
 
@@ -55,6 +55,9 @@ def build(verbose: bool = False) -> str:
         ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-c",
          os.path.join(CSRC, "tgraph_builder.cpp"), "-o",
          os.path.join(BUILD_DIR, "tgraph_builder.o")] + inc,
+        ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-c",
+         os.path.join(CSRC, "layout.cpp"), "-o",
+         os.path.join(BUILD_DIR, "layout.o")] + inc,
     ]
     with concurrent.futures.ThreadPoolExecutor(len(jobs)) as ex:
         for out in ex.map(_run, jobs):
@@ -66,6 +69,7 @@ def build(verbose: bool = False) -> str:
                           os.path.join(BUILD_DIR, "noalloc.o"),
                           os.path.join(BUILD_DIR, "capi.o"),
                           os.path.join(BUILD_DIR, "tgraph_builder.o"),
+                          os.path.join(BUILD_DIR, "layout.o"),
                           "-Xlinker", "-rpath=" + os.path.join(cuda, "lib64")])
     os.replace(tmp, OUT)
     return OUT

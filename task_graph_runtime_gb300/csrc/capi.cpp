@@ -1,8 +1,9 @@
 // C ABI (include/mpk.h): graph construction, device encoding, weight
 // binding and step launches.
-#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -14,6 +15,7 @@
 #include "device_abi.h"
 #include "graph_state.h"
 #include "launch.h"
+#include "layout.h"
 #include "mpk.h"
 #include "tgraph_builder.h"
 
@@ -79,7 +81,7 @@ void encode(mpk_graph* g) {
     TaskDesc& d = g->h_tasks[p];
     d.kind = (int16_t)t.kind;
     d.launch = (uint8_t)bg.launch[p];
-    d.flags = 0;
+    d.flags = task_flags(bg, t.kind, t.tile);
     d.layer = (int16_t)t.layer;
     d.b = (int16_t)t.b;
     d.g = (int16_t)t.g;
@@ -120,48 +122,6 @@ void encode(mpk_graph* g) {
   }
   g->encoded = true;
 }
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
-                                  void*, const cuuint64_t*, const cuuint64_t*,
-                                  const cuuint32_t*, const cuuint32_t*,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn) return fn;
-  void* p = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                       cudaEnableDefault, &q) != cudaSuccess ||
-      q != cudaDriverEntryPointSuccess)
-    return nullptr;
-  fn = reinterpret_cast<EncodeTiledFn>(p);
-  return fn;
-}
-
-// bf16 matrix [rows][cols], boxes of 64 columns x 8 rows, 128-byte swizzle.
-mpk_status make_tmap(uint8_t* dst, const void* base, int rows, int cols) {
-  EncodeTiledFn fn = get_encode_fn();
-  if (!fn) return MPK_ERR_CUDA;
-  if (((uintptr_t)base) & 15u) return MPK_ERR_INVALID_ARG;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, 8};
-  cuuint32_t estr[2] = {1, 1};
-  CUtensorMap m;
-  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                  const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return MPK_ERR_INVALID_ARG;
-  std::memcpy(dst, &m, 128);
-  return MPK_OK;
-}
-
-int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
@@ -210,22 +170,22 @@ mpk_status mpk_build_tgraph(const mpk_model_shape* shape,
   cfg.batch = batch;
   cfg.num_workers = W;
   cfg.gemv_rows_per_task = t.gemv_rows_per_task;
+  cfg.mma_rows_per_task = t.mma_rows_per_task;
   cfg.attn_chunks = t.attn_chunks;
-  const mpk_model_shape& s = *shape;
-  if (s.hidden > 8192) return MPK_ERR_UNSUPPORTED;
-  if (s.chain_ffn == 0 && s.n_kv_heads > 0 && s.n_q_heads % s.n_kv_heads == 0) {
-    const int grp = s.n_q_heads / s.n_kv_heads;
-    if (s.head_dim % 32 || grp * (s.head_dim + 2) > 1024)
-      return MPK_ERR_UNSUPPORTED;
-  }
+  cfg.coarse_events = t.coarse_events ? 1 : 0;
   std::unique_ptr<mpk_graph> g(new (std::nothrow) mpk_graph());
   if (!g) return MPK_ERR_OOM;
   std::string err;
   mpk_status st = build_tgraph(cfg, &g->bg, &err);
   if (st != MPK_OK) return st;
+  static std::atomic<uint64_t> next_uid{1};
+  g->uid = next_uid.fetch_add(1);
   g->num_sched_sms = sched_sms;
   g->sched_warps_per_sm = sched_warps;
-  g->pages_req = t.smem_pages > 0 ? t.smem_pages : kDefaultPages;
+  if (t.smem_pages < 0 || t.smem_pages > 8) return MPK_ERR_INVALID_ARG;
+  g->pages_req = t.smem_pages;
+  g->pf_pages = t.l2_prefetch_pages == 0 ? kDefaultPfPages
+                                          : std::max(0, t.l2_prefetch_pages);
   if (const char* env = std::getenv("MPK_WAIT_TIMEOUT_MS")) {
     const long ms = std::strtol(env, nullptr, 10);
     if (ms > 0) g->timeout_ns = (uint64_t)ms * 1000000ull;
@@ -278,12 +238,17 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
   const bool chain = s.chain_ffn > 0;
   if (chain ? (!w->chain_w1 || !w->chain_w2) : !w->layers)
     return MPK_ERR_INVALID_ARG;
+  auto aligned = [](const void* p) { return ((uintptr_t)p & 15u) == 0; };
+  if (!aligned(w->embed) || !aligned(w->final_norm) || !aligned(w->lm_head))
+    return MPK_ERR_INVALID_ARG;
+  if (chain && (!aligned(w->chain_w1) || !aligned(w->chain_w2)))
+    return MPK_ERR_INVALID_ARG;
   if (!chain) {
     for (int l = 0; l < s.n_layers; ++l)
       for (int k = 0; k < MPK_LAYER_NTENSORS; ++k) {
         const bool need = s.qk_norm || (k != MPK_W_QNORM && k != MPK_W_KNORM);
-        if (need && !w->layers[l * MPK_LAYER_NTENSORS + k])
-          return MPK_ERR_INVALID_ARG;
+        const void* p = w->layers[l * MPK_LAYER_NTENSORS + k];
+        if (need && (!p || !aligned(p))) return MPK_ERR_INVALID_ARG;
       }
   }
   int dev = 0, sms = 0, optin = 0;
@@ -294,13 +259,12 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
   const int W = cfg.num_workers;
   if (W + g->num_sched_sms > sms) return MPK_ERR_NOT_CORESIDENT;
   const int B = cfg.batch;
-  int pages = g->pages_req;
-  const int limit = std::min(optin, kSmemLimit);
-  while (pages > 2 && smem_bytes(pages, B) > limit) --pages;
-  if (smem_bytes(pages, B) > limit || pages > 16) return MPK_ERR_UNSUPPORTED;
-  g->n_pages = pages;
-  g->smem = smem_bytes(pages, B);
+  SmemLayout sm{};
+  if (!smem_layout(g->bg, g->pages_req, std::min(optin, kSmemLimit), &sm))
+    return MPK_ERR_UNSUPPORTED;
+  g->smem = sm.total;
   CK(configure_kernels(g->smem));
+  if (megakernel_max_blocks_per_sm(g->smem) < 1) return MPK_ERR_NOT_CORESIDENT;
   g->device = dev;
 
   // graph encoding
@@ -313,107 +277,40 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
   const int S = g->num_sched_sms * g->sched_warps_per_sm;
   CK(g->d_counters.alloc(nE));
   CK(g->d_status.alloc(2));
+  CK(g->d_merge_cnt.alloc((size_t)merge_counters(g->bg)));
   CK(g->d_jit_hdr.alloc(W));
   CK(g->d_sched_hdr.alloc(S));
   CK(g->d_jit_slots.alloc((size_t)W * kJitCap));
   CK(g->d_sched_slots.alloc((size_t)S * kSchedCap));
 
   // activation workspace
-  const int h = s.hidden, d = s.head_dim, Hq = s.n_q_heads, Hkv = s.n_kv_heads;
-  const int grp = chain ? 1 : Hq / Hkv;
-  const int C = chain ? 0 : cfg.attn_chunks;
-  const int Nqkv = chain ? 0 : (Hq + 2 * Hkv) * d;
-  const int Fa = std::max(s.ffn, s.chain_ffn);
   ActLayout A{};
-  int64_t off = 0;
-  auto take = [&](int64_t bytes) {
-    const int64_t o = off;
-    off += align_up(bytes, 256);
-    return o;
-  };
-  A.o_h = take((int64_t)B * h * 2);
-  A.o_n1 = take((int64_t)B * h * 2);
-  A.o_qkv = take((int64_t)B * Nqkv * 2);
-  A.o_q = take((int64_t)B * Hq * d * 2);
-  A.o_opart = take((int64_t)B * Hkv * C * grp * (d + 2) * 4);
-  A.o_attn = take((int64_t)B * Hq * d * 2);
-  A.o_o = take((int64_t)B * h * 2);
-  A.o_hmid = take((int64_t)B * h * 2);
-  A.o_n2 = take((int64_t)B * h * 2);
-  A.o_act = take((int64_t)B * Fa * 2);
-  A.o_dout = take((int64_t)B * h * 2);
-  A.layer_stride = off;
-  const int nblocks = std::max(s.n_layers, 1) + 1;
-  const int n_lm = g->op_n.empty() ? 0 : g->op_n[g->op_n.size() - 2];
-  int64_t goff = 0;
-  A.global_block = A.layer_stride * nblocks;
-  A.g_nf = goff;
-  goff += align_up((int64_t)B * h * 2, 256);
-  A.g_z = goff;
-  goff += align_up((int64_t)B * h * 2, 256);
-  A.g_amax = goff;
-  goff += align_up((int64_t)B * n_lm * 8, 256);
-  CK(g->d_act.alloc((size_t)(A.global_block + goff)));
-  CK(cudaMemset(g->d_act.p, 0, (size_t)(A.global_block + goff)));
+  const int64_t act_bytes = act_layout(g->bg, &A);
+  CK(g->d_act.alloc((size_t)act_bytes));
+  CK(cudaMemset(g->d_act.p, 0, (size_t)act_bytes));
   A.base = g->d_act.p;
 
-  // RoPE table: cos/sin(pos * theta^(-2i/d)) evaluated in double
-  const int max_ctx = chain ? 1 : s.max_pages_per_seq * s.page_size;
+  // RoPE table
   if (!chain) {
-    std::vector<float> cs((size_t)max_ctx * (d / 2) * 2);
-    for (int p = 0; p < max_ctx; ++p)
-      for (int i = 0; i < d / 2; ++i) {
-        const double inv = std::pow((double)s.rope_theta, -2.0 * i / d);
-        const double ang = (double)p * inv;
-        cs[((size_t)p * (d / 2) + i) * 2] = (float)std::cos(ang);
-        cs[((size_t)p * (d / 2) + i) * 2 + 1] = (float)std::sin(ang);
-      }
+    std::vector<float> cs((size_t)rope_table_floats(s));
+    rope_table(s, cs.data());
     CK(g->d_rope.upload(cs));
   }
 
-  // weights: pointer table and tensor maps
+  // per-layer weight pointers
   const int L = s.n_layers;
-  const int n_maps = 4 * L + 3;
-  std::vector<uint8_t> maps((size_t)n_maps * 128, 0);
   std::vector<const uint16_t*> ptrs((size_t)std::max(L, 1) * MPK_LAYER_NTENSORS,
                                     nullptr);
-  mpk_status st;
-  for (int l = 0; l < L; ++l) {
-    const void* const* lw = w->layers + (size_t)l * MPK_LAYER_NTENSORS;
+  for (int l = 0; l < L; ++l)
     for (int k = 0; k < MPK_LAYER_NTENSORS; ++k)
-      ptrs[(size_t)l * MPK_LAYER_NTENSORS + k] =
-          static_cast<const uint16_t*>(lw[k]);
-    if ((st = make_tmap(&maps[(4 * l + TM_QKV) * 128], lw[MPK_W_QKV], Nqkv, h)) != MPK_OK) return st;
-    if ((st = make_tmap(&maps[(4 * l + TM_O) * 128], lw[MPK_W_O], h, Hq * d)) != MPK_OK) return st;
-    if ((st = make_tmap(&maps[(4 * l + TM_GU) * 128], lw[MPK_W_GATEUP], 2 * s.ffn, h)) != MPK_OK) return st;
-    if ((st = make_tmap(&maps[(4 * l + TM_DOWN) * 128], lw[MPK_W_DOWN], h, s.ffn)) != MPK_OK) return st;
-  }
-  if ((st = make_tmap(&maps[(4 * L) * 128], w->lm_head, s.vocab, h)) != MPK_OK) return st;
-  if (chain) {
-    if ((st = make_tmap(&maps[(4 * L + 1) * 128], w->chain_w1, s.chain_ffn, h)) != MPK_OK) return st;
-    if ((st = make_tmap(&maps[(4 * L + 2) * 128], w->chain_w2, h, s.chain_ffn)) != MPK_OK) return st;
-  }
-  CK(g->d_tmaps.upload(maps));
+      ptrs[(size_t)l * MPK_LAYER_NTENSORS + k] = static_cast<const uint16_t*>(
+          w->layers[(size_t)l * MPK_LAYER_NTENSORS + k]);
   CK(g->d_layer_ptrs.upload(ptrs));
 
   KernelParams& P = g->params;
   P = KernelParams{};
-  P.dims.L = L;
-  P.dims.h = h;
-  P.dims.Hq = Hq;
-  P.dims.Hkv = Hkv;
-  P.dims.d = d;
-  P.dims.F = s.ffn;
-  P.dims.V = s.vocab;
-  P.dims.chain_ffn = s.chain_ffn;
-  P.dims.qk_norm = s.qk_norm;
-  P.dims.eps = s.rms_eps;
-  P.dims.B = B;
-  P.dims.C = C;
-  P.dims.page_size = s.page_size;
-  P.dims.max_pages = s.max_pages_per_seq;
-  P.dims.n_lm_tiles = n_lm;
-  P.dims.max_ctx = max_ctx;
+  P.dims = make_dims(g->bg, g->pf_pages);
+  P.sm = sm;
   DevGraph& G = P.graph;
   G.tasks = g->d_tasks.p;
   G.events = g->d_events.p;
@@ -425,6 +322,7 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
   G.aot_off = g->d_aot_off.p;
   G.op_tasks = g->d_op_tasks.p;
   G.counters = g->d_counters.p;
+  G.merge_cnt = g->d_merge_cnt.p;
   G.jit_hdr = g->d_jit_hdr.p;
   G.jit_slots = g->d_jit_slots.p;
   G.sched_hdr = g->d_sched_hdr.p;
@@ -436,14 +334,15 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
   G.W = W;
   G.S = S;
   G.sched_warps_per_sm = g->sched_warps_per_sm;
-  G.n_pages = pages;
   P.w.embed = static_cast<const uint16_t*>(w->embed);
   P.w.final_norm = static_cast<const uint16_t*>(w->final_norm);
   P.w.lm_head = static_cast<const uint16_t*>(w->lm_head);
+  P.w.chain_w1 = static_cast<const uint16_t*>(w->chain_w1);
+  P.w.chain_w2 = static_cast<const uint16_t*>(w->chain_w2);
   P.w.layers = g->d_layer_ptrs.p;
-  P.w.tmaps = g->d_tmaps.p;
   P.w.rope_cs = g->d_rope.p;
   P.act = A;
+  (void)B;
   g->bound = true;
   return mpk_reset(g);
 }
@@ -454,6 +353,7 @@ mpk_status mpk_reset(mpk_graph* g) {
   CK(cudaDeviceSynchronize());
   CK(cudaMemset(g->d_counters.p, 0, g->d_counters.n * sizeof(uint32_t)));
   CK(cudaMemset(g->d_status.p, 0, g->d_status.n * sizeof(uint32_t)));
+  CK(cudaMemset(g->d_merge_cnt.p, 0, g->d_merge_cnt.n * sizeof(uint32_t)));
   CK(cudaMemset(g->d_jit_hdr.p, 0, g->d_jit_hdr.n * sizeof(RingHdr)));
   CK(cudaMemset(g->d_sched_hdr.p, 0, g->d_sched_hdr.n * sizeof(RingHdr)));
   CK(cudaMemset(g->d_jit_slots.p, 0, g->d_jit_slots.n * sizeof(uint64_t)));
@@ -493,7 +393,8 @@ mpk_status mpk_decode_step(mpk_graph* g, const int32_t* d_tokens,
   a.timeout_ns = g->timeout_ns;
   if (!chain) {
     if (!kv || !kv->k_pool || !kv->v_pool || !kv->page_table ||
-        !kv->seq_lens || kv->num_pages < 1)
+        !kv->seq_lens || kv->num_pages < 1 ||
+        (((uintptr_t)kv->k_pool | (uintptr_t)kv->v_pool) & 15u))
       return MPK_ERR_INVALID_ARG;
     a.k_pool = static_cast<uint16_t*>(kv->k_pool);
     a.v_pool = static_cast<uint16_t*>(kv->v_pool);
@@ -616,6 +517,21 @@ mpk_status mpk_debug_read_trace(mpk_graph* g, uint64_t* host_records,
                   cudaMemcpyDeviceToHost));
   CK(cudaMemset(g->d_trace_count.p, 0, sizeof(uint32_t)));
   *n_records = take;
+  return MPK_OK;
+}
+
+mpk_status mpk_debug_read_hidden(mpk_graph* g, int layer, uint16_t* host_out) {
+  if (!g || !host_out) return MPK_ERR_INVALID_ARG;
+  if (!g->bound) return MPK_ERR_NOT_BOUND;
+  const mpk_model_shape& s = g->bg.cfg.shape;
+  if (s.chain_ffn > 0 || layer < 0 || layer > s.n_layers)
+    return MPK_ERR_INVALID_ARG;
+  CK(cudaDeviceSynchronize());
+  const KernelParams& P = g->params;
+  const char* src = P.act.base + (int64_t)layer * P.act.layer_stride + P.act.o_h;
+  CK(cudaMemcpy(host_out, src,
+                (size_t)g->bg.cfg.batch * s.hidden * sizeof(uint16_t),
+                cudaMemcpyDeviceToHost));
   return MPK_OK;
 }
 

@@ -3,7 +3,7 @@
 // task descriptors, events as {count, first, last}) and the launch
 // parameters.  MPK: A Compiler and Runtime for Mega-Kernelizing Tensor
 // Programs, §2 Q2 ("compact device-memory structure") and "关键实现细节" 2
-// (fixed-size task descriptors).
+// (fixed-size task descriptors, prefetched into shared memory).
 #pragma once
 
 #include <stdint.h>
@@ -14,18 +14,21 @@ namespace mpk {
 struct TaskDesc {
   int16_t kind;     // MPK_TASK_*
   uint8_t launch;   // MPK_LAUNCH_*
-  uint8_t flags;
+  uint8_t flags;    // TASK_F_*
   int16_t layer;
-  int16_t b;        // attention family: sequence
+  int16_t b;        // attention: sequence
   int32_t dep;      // the one event this task waits on
   int32_t trig;     // the one event this task triggers
   int32_t row0;     // MatMul: output rows [row0, row1)
   int32_t row1;
-  int16_t g;        // KV head
-  int16_t c;        // KV chunk
+  int16_t g;        // attention: KV head
+  int16_t c;        // attention: KV chunk
   int32_t tile;     // tile index within the operator
 };
 static_assert(sizeof(TaskDesc) == 32, "task descriptor must stay 32 bytes");
+
+// Tile 0 of a MatMul whose prologue forms a residual sum also stores it.
+enum : uint8_t { TASK_F_RESIDUAL = 1u };
 
 enum : uint32_t { EV_HAS_JIT = 1u, EV_HAS_INLINE = 2u };
 
@@ -49,15 +52,40 @@ struct RingHdr {
   uint32_t pad1[31];
 };
 
+// Weight pages: 8 matrix rows x up to 2048 columns, each row one
+// contiguous bulk copy, rows kPagePitch bytes apart (16 bytes of skew per
+// row keep ldmatrix reads of 8 rows free of bank conflicts).
+constexpr int kPageRows = 8;
+constexpr int kSegCols = 2048;
+constexpr int kPagePitch = kSegCols * 2 + 16;          // 4112
+constexpr int kPageBytes = kPageRows * kPagePitch;     // 32896
+constexpr int kAttnMaxTokens = 128;                    // per prefetched chunk
+
+// Byte offsets of the regions of a worker CTA's dynamic shared memory.
+struct SmemLayout {
+  int n_pages;      // ring slots of kPageBytes
+  int xs;           // activation staging / attention scratch
+  int xs_bytes;
+  int res;          // MatMul row results (fp32)
+  int res_floats;
+  int bars;         // full[n_pages], empty[n_pages] mbarriers
+  int ctrl;         // control words + staged task descriptors
+  int scratch;      // small reductions (1 KB)
+  int total;
+};
+
 // Shape and geometry the kernels need.
 struct Dims {
   int L, h, Hq, Hkv, d, F, V, chain_ffn, qk_norm;
   float eps;
-  int B;            // batch
-  int C;            // split-KV chunks per (sequence, KV head)
+  float attn_scale;  // 1/sqrt(d), rounded once from double on the host
+  int B;             // batch
+  int C;             // split-KV chunks per (sequence, KV head)
   int page_size, max_pages;
   int n_lm_tiles;
-  int max_ctx;      // rows of the RoPE table
+  int max_ctx;       // rows of the RoPE table
+  int kmax;          // longest MatMul reduction (x staging at batch 1)
+  int pf_pages;      // weight pages prefetched into L2 ahead of the ring
 };
 
 // Activation workspace: one block per layer (identical layout), plus a
@@ -65,9 +93,8 @@ struct Dims {
 struct ActLayout {
   char* base;
   int64_t layer_stride;
-  int64_t o_h, o_n1, o_qkv, o_q, o_opart, o_attn, o_o, o_hmid, o_n2, o_act,
-      o_dout;
-  int64_t g_nf, g_z, g_amax;   // offsets from the global block
+  int64_t o_h, o_qkv, o_opart, o_attn, o_o, o_hmid, o_act, o_dout;
+  int64_t g_z, g_amax;         // offsets from the global block
   int64_t global_block;        // offset of the global block from base
 };
 
@@ -80,6 +107,7 @@ struct DevGraph {
   const int32_t* aot_off;      // [W + 1]
   const int32_t* op_tasks;     // per operator, linear ids in tile order
   uint32_t* counters;          // [n_events]
+  uint32_t* merge_cnt;         // [L][B][Hkv] attention chunk arrivals
   RingHdr* jit_hdr;            // [W]
   uint64_t* jit_slots;         // [W][jit_cap]
   RingHdr* sched_hdr;          // [S]
@@ -93,21 +121,17 @@ struct DevGraph {
   int W;                       // worker CTAs
   int S;                       // scheduler warps in total
   int sched_warps_per_sm;
-  int n_pages;                 // shared-memory pages per worker
 };
 
 struct WeightPtrs {
   const uint16_t* embed;
   const uint16_t* final_norm;
   const uint16_t* lm_head;
+  const uint16_t* chain_w1;
+  const uint16_t* chain_w2;
   const uint16_t* const* layers;   // device array [L][MPK_LAYER_NTENSORS]
-  const uint8_t* tmaps;            // device array of 128-byte tensor maps
   const float* rope_cs;            // [max_ctx][d/2][2] (cos, sin)
 };
-
-// Tensor-map slots: layer l uses 4l + {0 qkv, 1 o, 2 gate-up, 3 down};
-// then lm_head, chain W1, chain W2.
-enum { TM_QKV = 0, TM_O = 1, TM_GU = 2, TM_DOWN = 3 };
 
 struct StepArgs {
   const int32_t* tokens;
@@ -124,6 +148,7 @@ struct StepArgs {
 
 struct KernelParams {
   Dims dims;
+  SmemLayout sm;
   DevGraph graph;
   WeightPtrs w;
   ActLayout act;

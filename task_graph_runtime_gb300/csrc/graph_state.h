@@ -14,7 +14,7 @@ namespace mpk_detail {
 
 constexpr uint32_t kJitCap = 1024;
 constexpr uint32_t kSchedCap = 4096;
-constexpr int kDefaultPages = 6;
+constexpr int kDefaultPfPages = 8;
 constexpr int kSmemLimit = 232448;   // 227 KB per block on sm_100-class
 
 template <typename T>
@@ -47,8 +47,9 @@ using mpk_detail::DevBuf;
 
 struct mpk_graph {
   mpk::BuiltGraph bg;
-  int num_sched_sms = 4, sched_warps_per_sm = 4,
-      pages_req = mpk_detail::kDefaultPages;
+  uint64_t uid = 0;   // build number, unique within the process
+  int num_sched_sms = 4, sched_warps_per_sm = 4, pages_req = 0,
+      pf_pages = mpk_detail::kDefaultPfPages;
   // export arrays (linear order)
   std::vector<int32_t> x_kind, x_op, x_layer, x_tile, x_row0, x_row1, x_b,
       x_g, x_c, x_pre, op_kind, op_layer, op_n;
@@ -61,17 +62,16 @@ struct mpk_graph {
   DevBuf<mpk::TaskDesc> d_tasks;
   DevBuf<mpk::EventDesc> d_events;
   DevBuf<int32_t> d_aot, d_aot_off, d_op_tasks;
-  DevBuf<uint32_t> d_counters, d_status;
+  DevBuf<uint32_t> d_counters, d_status, d_merge_cnt;
   DevBuf<mpk::RingHdr> d_jit_hdr, d_sched_hdr;
   DevBuf<uint64_t> d_jit_slots, d_sched_slots;
   DevBuf<char> d_act;
-  DevBuf<uint8_t> d_tmaps;
   DevBuf<const uint16_t*> d_layer_ptrs;
   DevBuf<float> d_rope;
   DevBuf<uint64_t> d_trace;
   DevBuf<uint32_t> d_trace_count;
   mpk::KernelParams params{};
-  int smem = 0, n_pages = 0;
+  int smem = 0;
   uint32_t epoch = 0;
   uint64_t timeout_ns = 2000000000ull;
   int mode = MPK_MODE_MEGAKERNEL;

@@ -8,16 +8,23 @@
 //   "Why this launch config (Table 1)" -- scheduler SMs x warps, 32 KB
 //     shared-memory pages;
 //   Figure 2 / "Optimization techniques inventory" -- cross-task software
-//     pipelining: weight pages of the NEXT tasks stream in (TMA) while the
-//     current task computes, and before the next task's event has fired,
-//     because weights never depend on an event.
+//     pipelining: the NEXT tasks' operands stream in while the current task
+//     computes, and before the next task's event has fired, because weights
+//     (and the KV cache of earlier tokens) never depend on an event;
+//   "关键实现细节" 2 -- task descriptors prefetched before dequeue.
 //
 // GB300 layout of a worker CTA (one per SM, 288 threads):
-//   warp 8      -- producer: walks this worker's AOT task list and issues
-//                  2-D TMA loads (cp.async.bulk.tensor, 128-byte swizzle) of
-//                  weight tiles into a ring of 32 KB pages;
+//   warp 8      -- producer: walks this worker's AOT task list.  Weight
+//                  pages (8 matrix rows x <= 2048 columns) arrive by one
+//                  contiguous 1-D bulk copy (cp.async.bulk) per row; AOT
+//                  attention tasks get their KV chunk the same way.  A
+//                  second cursor runs `pf_pages` pages further ahead and
+//                  prefetches them into L2 (cp.async.bulk.prefetch.L2), so
+//                  HBM keeps streaming while the ring is full at an event;
 //   warps 0..7  -- consumers: poll events and the JIT queue, run task bodies,
 //                  release pages, trigger events.
+// MatMul tiles run on CUDA cores at batch < 8 and on tensor cores
+// (mma.sync m16n8k16, batch as M, 8 weight rows as N) at batch >= 8.
 // Every spin-wait is bounded by %globaltimer; on timeout the kernel latches
 // MPK_ERR_TIMEOUT, raises an abort flag, drains its own copies in flight and
 // returns.
@@ -33,18 +40,8 @@ namespace mpk {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
-constexpr int kPageBytes = 32768;
-constexpr int kXsBytes = 32768;
-constexpr int kPageCols = 256;   // 4 TMA boxes of 64 bf16 columns
-constexpr int kMaxPageRows = 64;
-constexpr int kBoxRows = 8;      // one TMA box = 8 rows x 128 bytes = 1 KB
-constexpr int kCtrlBytes = 64;
-constexpr int kScratchBytes = 1024;
-
-__host__ __device__ inline int smem_bytes_for(int n_pages, int batch) {
-  return n_pages * kPageBytes + kXsBytes + 4 * kMaxPageRows * batch * 4 +
-         16 * n_pages + kCtrlBytes + kScratchBytes;
-}
+constexpr int kMaxRingPages = 8;
+constexpr unsigned kFull = 0xffffffffu;
 
 // ------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -81,15 +78,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap,
-                                            uint64_t* bar, int x, int y,
-                                            uint64_t policy) {
+// 1-D bulk copy global -> this CTA's shared memory, completion counted in
+// bytes on `bar`.  Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src,
+                                         uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_"
-      "tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
-          smem_addr(dst)),
-      "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::"
+      "cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src),
+               "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t p;
@@ -152,6 +155,26 @@ __device__ __forceinline__ uint64_t globaltimer() {
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0,
+                                        uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(addr)
+      : "memory");
+}
+// D += A (16x16 bf16, row) * B (16x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0,
+                                          uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 // ------------------------------------------------------------ bf16 helpers
 __device__ __forceinline__ float bf_lo(uint32_t w) {
@@ -170,24 +193,28 @@ __device__ __forceinline__ float round_bf(float f) { return bf2f(f2bf(f)); }
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
   return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
 }
+// acc + sum of 8 products, one fresh partial per 8 columns.
 __device__ __forceinline__ float dot8(uint4 w, uint4 x, float acc) {
-  acc = fmaf(bf_lo(w.x), bf_lo(x.x), acc);
-  acc = fmaf(bf_hi(w.x), bf_hi(x.x), acc);
-  acc = fmaf(bf_lo(w.y), bf_lo(x.y), acc);
-  acc = fmaf(bf_hi(w.y), bf_hi(x.y), acc);
-  acc = fmaf(bf_lo(w.z), bf_lo(x.z), acc);
-  acc = fmaf(bf_hi(w.z), bf_hi(x.z), acc);
-  acc = fmaf(bf_lo(w.w), bf_lo(x.w), acc);
-  acc = fmaf(bf_hi(w.w), bf_hi(x.w), acc);
-  return acc;
+  float p = bf_lo(w.x) * bf_lo(x.x);
+  p = fmaf(bf_hi(w.x), bf_hi(x.x), p);
+  p = fmaf(bf_lo(w.y), bf_lo(x.y), p);
+  p = fmaf(bf_hi(w.y), bf_hi(x.y), p);
+  p = fmaf(bf_lo(w.z), bf_lo(x.z), p);
+  p = fmaf(bf_hi(w.z), bf_hi(x.z), p);
+  p = fmaf(bf_lo(w.w), bf_lo(x.w), p);
+  p = fmaf(bf_hi(w.w), bf_hi(x.w), p);
+  return acc + p;
 }
 __device__ __forceinline__ float silu_f(float z) {
   return z / (1.0f + expf(-z));
 }
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
+}
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
 }
 
 // ------------------------------------------------------------ error latch
@@ -202,36 +229,36 @@ __device__ __forceinline__ bool aborted(const KernelParams& P) {
 
 // ------------------------------------------------------------ shared memory
 struct Smem {
-  uint8_t* pages;
-  uint16_t* xs;
-  float* red;
+  uint8_t* ring;
+  uint16_t* xs;       // activation staging (bf16) / attention scratch
+  float* res;         // MatMul row results
   uint64_t* full;
   uint64_t* empty;
-  volatile int* ctrl;
+  volatile int* ctrl; // [0..1] command, [2] bail-out, [3] aborted at entry,
+                      // [4] last-chunk flag
+  TaskDesc* desc;     // [0..1] staged descriptors, [2] the head AOT task's
+  uint64_t* times;    // [2] trace: looked-for, ready
   float* scratch;
+  int n_pages;
 };
 
-__device__ __forceinline__ Smem carve(uint8_t* base, int n_pages, int B) {
+__device__ __forceinline__ Smem carve(uint8_t* base, const SmemLayout& L) {
   Smem s;
-  size_t off = 0;
-  s.pages = base;
-  off += (size_t)n_pages * kPageBytes;
-  s.xs = reinterpret_cast<uint16_t*>(base + off);
-  off += kXsBytes;
-  s.red = reinterpret_cast<float*>(base + off);
-  off += (size_t)4 * kMaxPageRows * B * 4;
-  s.full = reinterpret_cast<uint64_t*>(base + off);
-  off += 8 * n_pages;
-  s.empty = reinterpret_cast<uint64_t*>(base + off);
-  off += 8 * n_pages;
-  s.ctrl = reinterpret_cast<volatile int*>(base + off);
-  off += kCtrlBytes;
-  s.scratch = reinterpret_cast<float*>(base + off);
+  s.ring = base;
+  s.xs = reinterpret_cast<uint16_t*>(base + L.xs);
+  s.res = reinterpret_cast<float*>(base + L.res);
+  s.full = reinterpret_cast<uint64_t*>(base + L.bars);
+  s.empty = s.full + L.n_pages;
+  s.ctrl = reinterpret_cast<volatile int*>(base + L.ctrl);
+  s.desc = reinterpret_cast<TaskDesc*>(base + L.ctrl + 64);
+  s.times = reinterpret_cast<uint64_t*>(base + L.ctrl + 160);
+  s.scratch = reinterpret_cast<float*>(base + L.scratch);
+  s.n_pages = L.n_pages;
   return s;
 }
 
-// Position in the ring of weight pages, advanced identically by the
-// producer and by every consumer thread.
+// Position in the ring of pages, advanced identically by the producer and
+// by every consumer thread.
 struct Ring {
   uint32_t slot, phase;
   __device__ __forceinline__ void advance(int n) {
@@ -241,6 +268,39 @@ struct Ring {
     }
   }
 };
+__device__ __forceinline__ uint8_t* page_ptr(const Smem& S, uint32_t slot) {
+  return S.ring + (size_t)slot * kPageBytes;
+}
+
+// Bounded wait for a ring page, by every consumer thread (each observes the
+// mbarrier phase, which makes the bulk-copied bytes visible to it).  On
+// timeout or abort the thread records a bail-out and carries on without the
+// page (the step's result is void by then), so all consumer threads still
+// reach the same barriers and leave the loop together.
+__device__ __forceinline__ bool wait_full(const KernelParams& P,
+                                          const Smem& S, const Ring& ring,
+                                          uint64_t deadline) {
+  if (S.ctrl[2]) return false;
+  uint32_t spins = 0;
+  while (!mbar_try_wait(&S.full[ring.slot], ring.phase)) {
+    if ((++spins & 1023u) == 0u && (aborted(P) || globaltimer() > deadline)) {
+      if (!aborted(P)) raise_error(P, MPK_ERR_TIMEOUT);
+      S.ctrl[2] = 1;
+      return false;
+    }
+  }
+  return true;
+}
+// Release a page (one arrival per consumer warp).  A page that never arrived
+// is not released, so the producer cannot refill a slot that a copy may
+// still be writing.
+__device__ __forceinline__ void release_page(const Smem& S, Ring& ring,
+                                             bool have) {
+  if (__all_sync(kFull, have) && (threadIdx.x & 31) == 0)
+    mbar_arrive(&S.empty[ring.slot]);
+  __syncwarp();
+  ring.advance(S.n_pages);
+}
 
 // ------------------------------------------------------------ tensors
 __device__ __forceinline__ char* layer_base(const KernelParams& P, int l) {
@@ -249,34 +309,36 @@ __device__ __forceinline__ char* layer_base(const KernelParams& P, int l) {
 __device__ __forceinline__ char* global_base(const KernelParams& P) {
   return P.act.base + P.act.global_block;
 }
+template <typename T = uint16_t>
+__device__ __forceinline__ T* lt(const KernelParams& P, int l, int64_t off) {
+  return reinterpret_cast<T*>(layer_base(P, l) + off);
+}
 __device__ __forceinline__ const uint16_t* layer_w(const KernelParams& P,
                                                    int l, int which) {
   return P.w.layers[l * MPK_LAYER_NTENSORS + which];
 }
-__device__ __forceinline__ const void* tmap_at(const KernelParams& P,
-                                               int idx) {
-  return P.w.tmaps + (size_t)idx * 128;
-}
 
-// Geometry of one MatMul task: which tensor map, rows, K, and paging.
-struct Gemv {
-  int kind, layer;
-  int row0, rows;      // output rows [row0, row0 + rows)
-  int K;               // reduction length
-  int N;               // output width (ldo)
-  int dual;            // gate/up pair: rows r of the gate and F + r
-  int up_off;          // row offset of the up half (dual)
-  int tmap;            // tensor-map slot
-  const uint16_t* src; // activations [B][K]
-  int rb_rows;         // output rows per row-block (64, or 32 when dual)
-};
-
+// ------------------------------------------------------------ MatMul tiles
 __device__ __forceinline__ bool is_gemv(int kind) {
   return kind == MPK_TASK_QKV || kind == MPK_TASK_O ||
          kind == MPK_TASK_GATEUP || kind == MPK_TASK_DOWN ||
          kind == MPK_TASK_LM_HEAD || kind == MPK_TASK_CHAIN_UP ||
          kind == MPK_TASK_CHAIN_DOWN;
 }
+
+// Geometry of one MatMul task.  Its weight rows are streamed as pages of 8
+// matrix rows (dual gate/up tiles: 4 gate rows then the matching 4 up rows)
+// by at most 2048 columns.  Page order: row groups outer at batch 1 (the
+// whole activation row is staged once), column segments outer at batch > 1
+// (one segment of every sequence's activation is staged at a time).
+struct Gemv {
+  int kind, layer;
+  int row0, rows;       // output rows [row0, row0 + rows)
+  int K, N;             // reduction length, output width
+  int dual, up_off;
+  int ngroups, nsegs, seg_outer;
+  const uint16_t* W;
+};
 
 __device__ Gemv gemv_geom(const KernelParams& P, const TaskDesc& t) {
   const Dims& D = P.dims;
@@ -287,136 +349,171 @@ __device__ Gemv gemv_geom(const KernelParams& P, const TaskDesc& t) {
   g.rows = t.row1 - t.row0;
   g.dual = 0;
   g.up_off = 0;
-  g.rb_rows = kMaxPageRows;
   const int l = t.layer;
   switch (t.kind) {
     case MPK_TASK_QKV:
       g.K = D.h;
       g.N = (D.Hq + 2 * D.Hkv) * D.d;
-      g.tmap = 4 * l + TM_QKV;
-      g.src = reinterpret_cast<const uint16_t*>(layer_base(P, l) + P.act.o_n1);
+      g.W = layer_w(P, l, MPK_W_QKV);
       break;
     case MPK_TASK_O:
       g.K = D.Hq * D.d;
       g.N = D.h;
-      g.tmap = 4 * l + TM_O;
-      g.src =
-          reinterpret_cast<const uint16_t*>(layer_base(P, l) + P.act.o_attn);
+      g.W = layer_w(P, l, MPK_W_O);
       break;
     case MPK_TASK_GATEUP:
       g.K = D.h;
       g.N = D.F;
       g.dual = 1;
       g.up_off = D.F;
-      g.rb_rows = kMaxPageRows / 2;
-      g.tmap = 4 * l + TM_GU;
-      g.src = reinterpret_cast<const uint16_t*>(layer_base(P, l) + P.act.o_n2);
+      g.W = layer_w(P, l, MPK_W_GATEUP);
       break;
     case MPK_TASK_DOWN:
       g.K = D.F;
       g.N = D.h;
-      g.tmap = 4 * l + TM_DOWN;
-      g.src = reinterpret_cast<const uint16_t*>(layer_base(P, l) + P.act.o_act);
+      g.W = layer_w(P, l, MPK_W_DOWN);
       break;
     case MPK_TASK_LM_HEAD:
       g.K = D.h;
       g.N = D.V;
-      g.tmap = 4 * D.L;
-      g.src = reinterpret_cast<const uint16_t*>(
-          global_base(P) + (D.chain_ffn > 0 ? P.act.g_z : P.act.g_nf));
+      g.W = P.w.lm_head;
       break;
     case MPK_TASK_CHAIN_UP:
       g.K = D.h;
       g.N = D.chain_ffn;
-      g.tmap = 4 * D.L + 1;
-      g.src = reinterpret_cast<const uint16_t*>(layer_base(P, 0) + P.act.o_n1);
+      g.W = P.w.chain_w1;
       break;
     default:  // MPK_TASK_CHAIN_DOWN
       g.K = D.chain_ffn;
       g.N = D.h;
-      g.tmap = 4 * D.L + 2;
-      g.src = reinterpret_cast<const uint16_t*>(layer_base(P, 0) + P.act.o_act);
+      g.W = P.w.chain_w2;
       break;
   }
+  const int gsize = g.dual ? 4 : kPageRows;
+  g.ngroups = (g.rows + gsize - 1) / gsize;
+  g.nsegs = (g.K + kSegCols - 1) / kSegCols;
+  g.seg_outer = D.B > 1 ? 1 : 0;
   return g;
 }
 
-// Rows of row-block rb (output rows; a dual page holds them twice).
-__device__ __forceinline__ int rb_count(const Gemv& g) {
-  return (g.rows + g.rb_rows - 1) / g.rb_rows;
+__device__ __forceinline__ void page_coords(const Gemv& g, int p, int& j,
+                                            int& s) {
+  if (g.seg_outer) {
+    s = p / g.ngroups;
+    j = p - s * g.ngroups;
+  } else {
+    j = p / g.nsegs;
+    s = p - j * g.nsegs;
+  }
 }
-__device__ __forceinline__ int rb_len(const Gemv& g, int rb) {
-  return min(g.rb_rows, g.rows - rb * g.rb_rows);
-}
-__device__ __forceinline__ int kpages(const Gemv& g) {
-  return (g.K + kPageCols - 1) / kPageCols;
+// Weight-matrix row held in row i (0..7) of group j's pages.
+__device__ __forceinline__ int page_wrow(const Gemv& g, int j, int i,
+                                         bool& valid) {
+  if (g.dual) {
+    const int o = 4 * j + (i & 3);
+    valid = o < g.rows;
+    return (i < 4 ? 0 : g.up_off) + g.row0 + o;
+  }
+  const int o = kPageRows * j + i;
+  valid = o < g.rows;
+  return g.row0 + o;
 }
 
 // ------------------------------------------------------------ producer
-// Streams the weight pages of one MatMul task into the ring.  All 32 lanes
-// of the producer warp take part; lane i issues box i of a page.
-__device__ bool produce_gemv(const KernelParams& P, const Smem& S,
-                             const Gemv& g, Ring& ring, uint32_t* issued,
-                             uint64_t deadline, uint64_t policy) {
+// Weight page p of a MatMul task: one bulk copy per valid row, issued by
+// lanes 0..7 after lane 0 posts the byte count.
+__device__ void issue_gemv_page(const Gemv& g, int p, uint8_t* page,
+                                uint64_t* bar, uint64_t policy) {
   const int lane = threadIdx.x & 31;
-  const int n_pages = P.graph.n_pages;
-  const void* tm = tmap_at(P, g.tmap);
-  const int nrb = rb_count(g), nkp = kpages(g);
-  for (int rb = 0; rb < nrb; ++rb) {
-    const int len = rb_len(g, rb);
-    const int r8 = (len + kBoxRows - 1) / kBoxRows;   // row boxes (per half)
-    const int prow8 = g.dual ? 2 * r8 : r8;
-    const int row_base = g.row0 + rb * g.rb_rows;
-    for (int cb = 0; cb < nkp; ++cb) {
-      const int c0 = cb * kPageCols;
-      const int nbc = min(4, (g.K - c0 + 63) / 64);
-      // wait until the consumers released this slot (lane 0 decides)
-      int ok = 1;
-      if (lane == 0) {
-        uint32_t spins = 0;
-        while (!mbar_try_wait(&S.empty[ring.slot], ring.phase ^ 1u)) {
-          if ((++spins & 1023u) == 0u &&
-              (aborted(P) || globaltimer() > deadline)) {
-            if (!aborted(P)) raise_error(P, MPK_ERR_TIMEOUT);
-            ok = 0;
-            break;
-          }
-        }
-        if (ok && aborted(P)) ok = 0;
-        if (ok)
-          mbar_arrive_expect_tx(&S.full[ring.slot],
-                                (uint32_t)(nbc * prow8 * 1024));
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) return false;
-      uint8_t* page = S.pages + (size_t)ring.slot * kPageBytes;
-      const int nbox = nbc * prow8;
-      for (int i = lane; i < nbox; i += 32) {
-        const int gb = i / prow8, rbi = i % prow8;
-        int y;
-        if (g.dual)
-          y = (rbi < r8) ? row_base + rbi * kBoxRows
-                         : g.up_off + row_base + (rbi - r8) * kBoxRows;
-        else
-          y = row_base + rbi * kBoxRows;
-        tma_load_2d(page + (size_t)(gb * prow8 + rbi) * 1024, tm,
-                    &S.full[ring.slot], c0 + gb * 64, y, policy);
-      }
-      issued[ring.slot] = 1u | (ring.phase << 1);
-      ring.advance(n_pages);
-      __syncwarp();
-    }
+  int j, s;
+  page_coords(g, p, j, s);
+  const int c0 = s * kSegCols;
+  const uint32_t bytes = (uint32_t)min(kSegCols, g.K - c0) * 2u;
+  bool valid = false;
+  int wr = 0;
+  if (lane < kPageRows) wr = page_wrow(g, j, lane, valid);
+  const uint32_t vmask = __ballot_sync(kFull, valid);
+  if (lane == 0) mbar_arrive_expect_tx(bar, __popc(vmask) * bytes);
+  __syncwarp();
+  if (valid)
+    bulk_g2s(page + lane * kPagePitch, g.W + (int64_t)wr * g.K + c0, bytes,
+             bar, policy);
+}
+__device__ void prefetch_gemv_page(const Gemv& g, int p) {
+  const int lane = threadIdx.x & 31;
+  if (lane >= kPageRows) return;
+  int j, s;
+  page_coords(g, p, j, s);
+  const int c0 = s * kSegCols;
+  bool valid;
+  const int wr = page_wrow(g, j, lane, valid);
+  if (valid)
+    prefetch_l2(g.W + (int64_t)wr * g.K + c0,
+                (uint32_t)min(kSegCols, g.K - c0) * 2u);
+}
+
+// Chunk c of (b, g) covers tokens [t0, t1) of the n = seq_len + 1 positions.
+__device__ __forceinline__ void chunk_range(int c, int n, int C, int& t0,
+                                            int& t1) {
+  t0 = (int)(((int64_t)c * n) / C);
+  t1 = (int)(((int64_t)(c + 1) * n) / C);
+}
+
+// KV chunk of an AOT attention task: the cached tokens [t0, min(t1, pos))
+// into the K page and the V page (token-major rows of d values), one bulk
+// copy per run of tokens inside one KV page.  Lane 0 only.
+__device__ void issue_attn_pages(const KernelParams& P, const TaskDesc& t,
+                                 uint8_t* kpage, uint64_t* kbar,
+                                 uint8_t* vpage, uint64_t* vbar,
+                                 uint64_t policy) {
+  const Dims& D = P.dims;
+  const int b = t.b, pos = __ldcg(P.step.seq_lens + b);
+  const int n = pos + 1;
+  int t0 = 0, t1 = 0;
+  bool ok = pos >= 0 && n <= D.max_ctx;
+  if (ok) chunk_range(t.c, n, D.C, t0, t1);
+  const int te = ok ? min(min(t1, pos), t0 + kAttnMaxTokens) : 0;
+  const int P_ = D.page_size, d = D.d;
+  const uint32_t row_bytes = (uint32_t)d * 2u;
+  const int32_t* pt = P.step.page_table + (int64_t)b * D.max_pages;
+  const int64_t head_elems = (int64_t)P_ * d;
+  const int64_t layer_elems =
+      (int64_t)t.layer * P.step.num_pages * D.Hkv * head_elems;
+  uint32_t total = 0;
+  for (int tok = t0; tok < te;) {
+    const int run_end = min(te, (tok / P_ + 1) * P_);
+    const int page = __ldg(pt + tok / P_);
+    if (page >= 0 && page < P.step.num_pages)
+      total += (uint32_t)(run_end - tok) * row_bytes;
+    else
+      raise_error(P, MPK_ERR_KV_PAGE);
+    tok = run_end;
   }
-  return true;
+  mbar_arrive_expect_tx(kbar, total);
+  mbar_arrive_expect_tx(vbar, total);
+  for (int tok = t0; tok < te;) {
+    const int run_end = min(te, (tok / P_ + 1) * P_);
+    const int page = __ldg(pt + tok / P_);
+    if (page >= 0 && page < P.step.num_pages) {
+      const int64_t off = layer_elems +
+                          ((int64_t)page * D.Hkv + t.g) * head_elems +
+                          (int64_t)(tok % P_) * d;
+      const uint32_t bytes = (uint32_t)(run_end - tok) * row_bytes;
+      const size_t dst = (size_t)(tok - t0) * row_bytes;
+      bulk_g2s(kpage + dst, P.step.k_pool + off, bytes, kbar, policy);
+      bulk_g2s(vpage + dst, P.step.v_pool + off, bytes, vbar, policy);
+    }
+    tok = run_end;
+  }
 }
 
 // After an abort: wait (bounded) until every copy this producer issued has
-// landed, so no TMA writes into shared memory after the CTA exits.
+// landed, so no bulk copy writes into shared memory after the CTA exits.
 __device__ void drain_copies(const KernelParams& P, const Smem& S,
                              const uint32_t* issued) {
   if ((threadIdx.x & 31) != 0) return;
   const uint64_t limit = globaltimer() + 200000000ull;  // 200 ms
-  for (int s = 0; s < P.graph.n_pages; ++s) {
+  for (int s = 0; s < S.n_pages; ++s) {
     if (!(issued[s] & 1u)) continue;
     const uint32_t ph = (issued[s] >> 1) & 1u;
     while (!mbar_try_wait(&S.full[s], ph)) {
@@ -425,416 +522,1052 @@ __device__ void drain_copies(const KernelParams& P, const Smem& S,
   }
 }
 
-// ------------------------------------------------------------ task bodies
-// RMSNorm family: x = a + c (bf16, rounded) or an embedding row; writes x
-// (optional) and bf16((x * (mean(x^2) + eps)^-1/2) * w).
-__device__ void task_norm(const KernelParams& P, const Smem& S,
-                          const TaskDesc& t) {
-  const Dims& D = P.dims;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = D.h, l = t.layer;
-  const uint16_t *a = nullptr, *c = nullptr, *w;
-  uint16_t *out_h = nullptr, *out_n;
-  bool embed = false;
-  switch (t.kind) {
-    case MPK_TASK_NORM1:
-      w = layer_w(P, l, MPK_W_LN1);
-      out_h = reinterpret_cast<uint16_t*>(layer_base(P, l) + P.act.o_h);
-      out_n = reinterpret_cast<uint16_t*>(layer_base(P, l) + P.act.o_n1);
-      if (l == 0) {
-        embed = true;
-      } else {
-        a = reinterpret_cast<const uint16_t*>(layer_base(P, l - 1) +
-                                              P.act.o_hmid);
-        c = reinterpret_cast<const uint16_t*>(layer_base(P, l - 1) +
-                                              P.act.o_dout);
-      }
-      break;
-    case MPK_TASK_NORM2:
-      w = layer_w(P, l, MPK_W_LN2);
-      a = reinterpret_cast<const uint16_t*>(layer_base(P, l) + P.act.o_h);
-      c = reinterpret_cast<const uint16_t*>(layer_base(P, l) + P.act.o_o);
-      out_h = reinterpret_cast<uint16_t*>(layer_base(P, l) + P.act.o_hmid);
-      out_n = reinterpret_cast<uint16_t*>(layer_base(P, l) + P.act.o_n2);
-      break;
-    case MPK_TASK_FINAL_NORM:
-      w = P.w.final_norm;
-      a = reinterpret_cast<const uint16_t*>(layer_base(P, D.L - 1) +
-                                            P.act.o_hmid);
-      c = reinterpret_cast<const uint16_t*>(layer_base(P, D.L - 1) +
-                                            P.act.o_dout);
-      out_h = reinterpret_cast<uint16_t*>(layer_base(P, D.L) + P.act.o_h);
-      out_n = reinterpret_cast<uint16_t*>(global_base(P) + P.act.g_nf);
-      break;
-    default:  // MPK_TASK_CHAIN_NORM
-      w = P.w.final_norm;
-      embed = true;
-      out_n = reinterpret_cast<uint16_t*>(layer_base(P, 0) + P.act.o_n1);
-      break;
+// Pages a task takes from the ring (0 for tasks that use none).
+__device__ __forceinline__ int ring_pages_of(const KernelParams& P,
+                                             const TaskDesc& t, Gemv* g) {
+  if (is_gemv(t.kind)) {
+    *g = gemv_geom(P, t);
+    return g->ngroups * g->nsegs;
   }
-  constexpr int kMaxChunks = 4;  // h <= 4 * 8 * 256 = 8192
-  const int nchunk = (h / 8 + kConsumers - 1) / kConsumers;
-  for (int b = 0; b < D.B; ++b) {
-    float x[kMaxChunks][8];
-    float ss = 0.f;
-    const uint16_t* erow = nullptr;
-    if (embed) {
-      int tok = __ldg(P.step.tokens + b);
-      tok = min(max(tok, 0), D.V - 1);
-      erow = P.w.embed + (int64_t)tok * h;
-    }
-#pragma unroll
-    for (int k = 0; k < kMaxChunks; ++k) {
-      const int i = (tid + k * kConsumers) * 8;
-      if (k < nchunk && i < h) {
-        if (embed) {
-          uint4 v = __ldg(reinterpret_cast<const uint4*>(erow + i));
-          const uint32_t* pw = &v.x;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            x[k][2 * q] = bf_lo(pw[q]);
-            x[k][2 * q + 1] = bf_hi(pw[q]);
-          }
-        } else {
-          uint4 va = __ldcg(reinterpret_cast<const uint4*>(a + (int64_t)b * h + i));
-          uint4 vc = __ldcg(reinterpret_cast<const uint4*>(c + (int64_t)b * h + i));
-          const uint32_t* pa = &va.x;
-          const uint32_t* pc = &vc.x;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            x[k][2 * q] = round_bf(__fadd_rn(bf_lo(pa[q]), bf_lo(pc[q])));
-            x[k][2 * q + 1] = round_bf(__fadd_rn(bf_hi(pa[q]), bf_hi(pc[q])));
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) ss = fmaf(x[k][q], x[k][q], ss);
-      }
-    }
-    ss = warp_sum(ss);
-    if (lane == 0) S.scratch[warp] = ss;
-    consumer_sync();
-    float tot = 0.f;
-#pragma unroll
-    for (int q = 0; q < kConsumerWarps; ++q) tot += S.scratch[q];
-    const float r = 1.0f / sqrtf(tot / (float)h + D.eps);
-#pragma unroll
-    for (int k = 0; k < kMaxChunks; ++k) {
-      const int i = (tid + k * kConsumers) * 8;
-      if (k < nchunk && i < h) {
-        uint4 wv = __ldg(reinterpret_cast<const uint4*>(w + i));
-        const uint32_t* pw = &wv.x;
-        uint4 on, oh;
-        uint32_t* pon = &on.x;
-        uint32_t* poh = &oh.x;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float n0 = __fmul_rn(__fmul_rn(x[k][2 * q], r), bf_lo(pw[q]));
-          const float n1 = __fmul_rn(__fmul_rn(x[k][2 * q + 1], r), bf_hi(pw[q]));
-          pon[q] = pack_bf2(n0, n1);
-          poh[q] = pack_bf2(x[k][2 * q], x[k][2 * q + 1]);
-        }
-        *reinterpret_cast<uint4*>(out_n + (int64_t)b * h + i) = on;
-        if (out_h) *reinterpret_cast<uint4*>(out_h + (int64_t)b * h + i) = oh;
-      }
-    }
-    consumer_sync();   // scratch reuse across rows
-  }
+  if (t.kind == MPK_TASK_ATTN && t.launch == MPK_LAUNCH_AOT) return 2;
+  return 0;
 }
 
-// q/k RMSNorm (optional) + RoPE for the query heads of KV head g and for
-// its key; appends k, v at position seq_lens[b] of the paged cache.
-__device__ void task_rope(const KernelParams& P, const Smem& S,
-                          const TaskDesc& t) {
-  const Dims& D = P.dims;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = t.b, g = t.g, l = t.layer, d = D.d, half = d / 2;
-  const int grp = D.Hq / D.Hkv;
-  const int pos = __ldcg(P.step.seq_lens + b);
-  const int pidx = pos / D.page_size;
-  int page = -1;
-  if (pos >= 0 && pidx < D.max_pages)
-    page = __ldg(P.step.page_table + (int64_t)b * D.max_pages + pidx);
-  if (page < 0 || page >= P.step.num_pages || pos >= D.max_ctx) {
-    if (threadIdx.x == 0) raise_error(P, MPK_ERR_KV_PAGE);
-    return;
+// Bounded wait for a free ring slot by lane 0; every lane then observes the
+// released phase before any copy into the slot is issued.
+__device__ __forceinline__ bool wait_empty(const KernelParams& P,
+                                           const Smem& S, const Ring& ring,
+                                           uint64_t deadline) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) {
+    uint32_t spins = 0;
+    while (!mbar_try_wait(&S.empty[ring.slot], ring.phase ^ 1u)) {
+      if ((++spins & 1023u) == 0u &&
+          (aborted(P) || globaltimer() > deadline)) {
+        if (!aborted(P)) raise_error(P, MPK_ERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+    }
+    if (ok && aborted(P)) ok = 0;
   }
-  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(
-      layer_base(P, l) + P.act.o_qkv) + (int64_t)b * (D.Hq + 2 * D.Hkv) * d;
-  uint16_t* qout = reinterpret_cast<uint16_t*>(layer_base(P, l) + P.act.o_q) +
-                   (int64_t)b * D.Hq * d;
-  const int64_t slot = ((((int64_t)l * P.step.num_pages + page) * D.Hkv + g) *
-                            D.page_size + pos % D.page_size) * d;
-  const float* cs = P.w.rope_cs + (int64_t)pos * half * 2;
-  for (int hh = warp; hh < grp + 2; hh += kConsumerWarps) {
-    const uint16_t* src;
-    uint16_t* dst;
-    const uint16_t* nw = nullptr;
-    bool rot = true;
-    if (hh < grp) {
-      src = qkv + (int64_t)(g * grp + hh) * d;
-      dst = qout + (int64_t)(g * grp + hh) * d;
-      if (D.qk_norm) nw = layer_w(P, l, MPK_W_QNORM);
-    } else if (hh == grp) {
-      src = qkv + (int64_t)(D.Hq + g) * d;
-      dst = P.step.k_pool + slot;
-      if (D.qk_norm) nw = layer_w(P, l, MPK_W_KNORM);
-    } else {
-      src = qkv + (int64_t)(D.Hq + D.Hkv + g) * d;
-      dst = P.step.v_pool + slot;
-      rot = false;
+  ok = __shfl_sync(kFull, ok, 0);
+  if (ok) (void)mbar_try_wait(&S.empty[ring.slot], ring.phase ^ 1u);
+  return ok != 0;
+}
+
+// The L2 look-ahead cursor walks the same page sequence as the ring.
+struct Lookahead {
+  int i;        // index into the task list
+  int p, np;    // page within that task, pages of that task (-1: not read)
+  int64_t count;
+  Gemv g;
+  bool gemv;
+};
+
+__device__ void lookahead(const KernelParams& P, const int32_t* list, int n,
+                          Lookahead& la, int64_t limit) {
+  while (la.count < limit && la.i < n) {
+    if (la.np < 0) {
+      const TaskDesc t = P.graph.tasks[list[la.i]];
+      la.np = ring_pages_of(P, t, &la.g);
+      la.gemv = is_gemv(t.kind);
+      la.p = 0;
     }
-    // pairs (i, i + d/2) for i = lane, lane + 32 (half <= 64)
-    float x1[2], x2[2];
-    float ss = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = lane + 32 * k;
-      if (i < half) {
-        x1[k] = bf2f(__ldcg(src + i));
-        x2[k] = bf2f(__ldcg(src + i + half));
-        ss = fmaf(x1[k], x1[k], ss);
-        ss = fmaf(x2[k], x2[k], ss);
-      }
-    }
-    if (!rot) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int i = lane + 32 * k;
-        if (i < half) {
-          dst[i] = f2bf(x1[k]);
-          dst[i + half] = f2bf(x2[k]);
-        }
-      }
+    if (la.p >= la.np) {
+      ++la.i;
+      la.np = -1;
       continue;
     }
-    if (nw) {
-      ss = warp_sum(ss);
-      const float r = 1.0f / sqrtf(ss / (float)d + D.eps);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int i = lane + 32 * k;
-        if (i < half) {
-          x1[k] = round_bf(__fmul_rn(__fmul_rn(x1[k], r), bf2f(__ldg(nw + i))));
-          x2[k] = round_bf(
-              __fmul_rn(__fmul_rn(x2[k], r), bf2f(__ldg(nw + i + half))));
-        }
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = lane + 32 * k;
-      if (i < half) {
-        const float c = __ldg(cs + 2 * i), s = __ldg(cs + 2 * i + 1);
-        const float y1 = __fsub_rn(__fmul_rn(x1[k], c), __fmul_rn(x2[k], s));
-        const float y2 = __fadd_rn(__fmul_rn(x2[k], c), __fmul_rn(x1[k], s));
-        dst[i] = f2bf(y1);
-        dst[i + half] = f2bf(y2);
-      }
-    }
+    if (la.gemv) prefetch_gemv_page(la.g, la.p);
+    ++la.p;
+    ++la.count;
   }
 }
 
-// Paged attention over KV chunk c of (sequence b, KV head g): tokens
-// [c n / C, (c+1) n / C) of n = seq_lens[b] + 1.  Each warp runs an online
-// softmax over a strided subset of the tokens for all query heads of the
-// group; the warps are merged in shared memory into one partial
-// (m, l, acc[d]) per query head.
-template <int DL, int kMaxGrp>
-__device__ void attn_body(const KernelParams& P, const Smem& S,
-                          const TaskDesc& t) {
-  const Dims& D = P.dims;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = t.b, g = t.g, l = t.layer, d = D.d;
-  const int grp = D.Hq / D.Hkv;
-  const int n = __ldcg(P.step.seq_lens + b) + 1;
-  const int t0 = (int)(((int64_t)t.c * n) / D.C);
-  const int t1 = (int)(((int64_t)(t.c + 1) * n) / D.C);
-  const float scale = 1.0f / sqrtf((float)d);
-  const uint16_t* q = reinterpret_cast<const uint16_t*>(
-                          layer_base(P, l) + P.act.o_q) +
-                      (int64_t)b * D.Hq * d + (int64_t)g * grp * d;
-  float qr[kMaxGrp][DL];
-  float m[kMaxGrp], lsum[kMaxGrp], acc[kMaxGrp][DL];
+__device__ void producer_role(const KernelParams& P, const Smem& S,
+                              const int32_t* list, int n, uint64_t deadline) {
+  const int lane = threadIdx.x & 31;
+  uint32_t issued[kMaxRingPages];
 #pragma unroll
-  for (int hh = 0; hh < kMaxGrp; ++hh) {
-    m[hh] = -INFINITY;
-    lsum[hh] = 0.f;
-#pragma unroll
-    for (int e = 0; e < DL; ++e) {
-      acc[hh][e] = 0.f;
-      qr[hh][e] = (hh < grp) ? bf2f(__ldcg(q + hh * d + lane * DL + e)) : 0.f;
-    }
-  }
-  const int64_t head_stride = (int64_t)D.page_size * d;
-  const int64_t page_stride = (int64_t)D.Hkv * head_stride;
-  const int64_t layer_off = (int64_t)l * P.step.num_pages * page_stride +
-                            (int64_t)g * head_stride;
-  const int32_t* pt = P.step.page_table + (int64_t)b * D.max_pages;
-  for (int tok = t0 + warp; tok < t1; tok += kConsumerWarps) {
-    const int page = __ldg(pt + tok / D.page_size);
-    if (page < 0 || page >= P.step.num_pages) {
-      if (lane == 0) raise_error(P, MPK_ERR_KV_PAGE);
-      break;
-    }
-    const int64_t off = layer_off + (int64_t)page * page_stride +
-                        (int64_t)(tok % D.page_size) * d + lane * DL;
-    float kf[DL], vf[DL];
-    if (DL == 4) {
-      uint2 kv = __ldcg(reinterpret_cast<const uint2*>(P.step.k_pool + off));
-      uint2 vv = __ldcg(reinterpret_cast<const uint2*>(P.step.v_pool + off));
-      kf[0] = bf_lo(kv.x); kf[1] = bf_hi(kv.x);
-      kf[2 % DL] = bf_lo(kv.y); kf[3 % DL] = bf_hi(kv.y);
-      vf[0] = bf_lo(vv.x); vf[1] = bf_hi(vv.x);
-      vf[2 % DL] = bf_lo(vv.y); vf[3 % DL] = bf_hi(vv.y);
-    } else if (DL == 2) {
-      uint32_t kv = __ldcg(reinterpret_cast<const unsigned int*>(P.step.k_pool + off));
-      uint32_t vv = __ldcg(reinterpret_cast<const unsigned int*>(P.step.v_pool + off));
-      kf[0] = bf_lo(kv); kf[1 % DL] = bf_hi(kv);
-      vf[0] = bf_lo(vv); vf[1 % DL] = bf_hi(vv);
+  for (int i = 0; i < kMaxRingPages; ++i) issued[i] = 0;
+  Ring ring{0, 0};
+  const uint64_t policy = evict_first_policy();
+  const int pf = P.dims.pf_pages;
+  Lookahead la{0, 0, -1, 0, Gemv{}, false};
+  int64_t copied = 0;
+  for (int i = 0; i < n; ++i) {
+    const TaskDesc t = P.graph.tasks[list[i]];
+    Gemv g;
+    const int np = ring_pages_of(P, t, &g);
+    if (np == 0) continue;
+    if (is_gemv(t.kind)) {
+      for (int p = 0; p < np; ++p) {
+        if (pf > 0) lookahead(P, list, n, la, copied + 1 + pf);
+        if (!wait_empty(P, S, ring, deadline)) {
+          drain_copies(P, S, issued);
+          return;
+        }
+        issue_gemv_page(g, p, page_ptr(S, ring.slot), &S.full[ring.slot],
+                        policy);
+        issued[ring.slot] = 1u | (ring.phase << 1);
+        ring.advance(S.n_pages);
+        ++copied;
+      }
     } else {
-#pragma unroll
-      for (int e = 0; e < DL; ++e) {
-        kf[e] = bf2f(__ldcg(P.step.k_pool + off + e));
-        vf[e] = bf2f(__ldcg(P.step.v_pool + off + e));
+      // attention: K page then V page
+      if (pf > 0) lookahead(P, list, n, la, copied + 2 + pf);
+      if (!wait_empty(P, S, ring, deadline)) {
+        drain_copies(P, S, issued);
+        return;
       }
-    }
-#pragma unroll
-    for (int hh = 0; hh < kMaxGrp; ++hh) {
-      if (hh < grp) {
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < DL; ++e) s = fmaf(qr[hh][e], kf[e], s);
-        s = warp_sum(s) * scale;
-        const float mn = fmaxf(m[hh], s);
-        const float corr = expf(m[hh] - mn);
-        const float p = expf(s - mn);
-        lsum[hh] = lsum[hh] * corr + p;
-#pragma unroll
-        for (int e = 0; e < DL; ++e) acc[hh][e] = fmaf(p, vf[e], acc[hh][e] * corr);
-        m[hh] = mn;
+      const uint32_t ks = ring.slot;
+      issued[ring.slot] = 1u | (ring.phase << 1);
+      ring.advance(S.n_pages);
+      if (!wait_empty(P, S, ring, deadline)) {
+        // the K slot was claimed but nothing was copied into it: complete
+        // its phase so the drain below does not wait on it
+        if (lane == 0) mbar_arrive_expect_tx(&S.full[ks], 0);
+        drain_copies(P, S, issued);
+        return;
       }
+      const uint32_t vs = ring.slot;
+      issued[ring.slot] = 1u | (ring.phase << 1);
+      ring.advance(S.n_pages);
+      if (lane == 0)
+        issue_attn_pages(P, t, page_ptr(S, ks), &S.full[ks], page_ptr(S, vs),
+                         &S.full[vs], policy);
+      __syncwarp();
+      copied += 2;
     }
   }
-  // merge the 8 warps: layout [warp][grp][2 + d] floats in the x area
-  float* wbuf = reinterpret_cast<float*>(S.xs);
-  const int rec = 2 + d;
-#pragma unroll
-  for (int hh = 0; hh < kMaxGrp; ++hh) {
-    if (hh < grp) {
-      float* r = wbuf + ((int64_t)warp * grp + hh) * rec;
-      if (lane == 0) {
-        r[0] = m[hh];
-        r[1] = lsum[hh];
+  // the consumers wait for every page before leaving, so all copies have
+  // landed by the time the CTA exits unless the step aborted
+  if (aborted(P)) drain_copies(P, S, issued);
+}
+
+// ------------------------------------------------------------ x staging
+// Where a MatMul tile's activation row comes from.  Norm modes form the
+// residual sum (or gather the embedding row), round it to bf16, and RMSNorm
+// it with `gain`; tile 0 also stores the residual for later operators.
+enum { X_PLAIN = 0, X_NORM_ADD = 1, X_NORM_EMBED = 2 };
+struct XSrc {
+  int mode;
+  const uint16_t* a;      // plain source, or first addend
+  const uint16_t* c;      // second addend
+  const uint16_t* gain;
+  uint16_t* resid;        // residual output (tile 0 only), else null
+};
+
+__device__ XSrc x_source(const KernelParams& P, const TaskDesc& t) {
+  const Dims& D = P.dims;
+  const int l = t.layer;
+  const bool res = (t.flags & TASK_F_RESIDUAL) != 0;
+  XSrc x{X_PLAIN, nullptr, nullptr, nullptr, nullptr};
+  switch (t.kind) {
+    case MPK_TASK_QKV:
+      x.gain = layer_w(P, l, MPK_W_LN1);
+      if (res) x.resid = lt(P, l, P.act.o_h);
+      if (l == 0) {
+        x.mode = X_NORM_EMBED;
+      } else {
+        x.mode = X_NORM_ADD;
+        x.a = lt(P, l - 1, P.act.o_hmid);
+        x.c = lt(P, l - 1, P.act.o_dout);
       }
+      break;
+    case MPK_TASK_O:
+      x.a = lt(P, l, P.act.o_attn);
+      break;
+    case MPK_TASK_GATEUP:
+      x.mode = X_NORM_ADD;
+      x.a = lt(P, l, P.act.o_h);
+      x.c = lt(P, l, P.act.o_o);
+      x.gain = layer_w(P, l, MPK_W_LN2);
+      if (res) x.resid = lt(P, l, P.act.o_hmid);
+      break;
+    case MPK_TASK_DOWN:
+      x.a = lt(P, l, P.act.o_act);
+      break;
+    case MPK_TASK_LM_HEAD:
+      if (D.chain_ffn > 0) {
+        x.a = reinterpret_cast<const uint16_t*>(global_base(P) + P.act.g_z);
+      } else {
+        x.mode = X_NORM_ADD;
+        x.a = lt(P, D.L - 1, P.act.o_hmid);
+        x.c = lt(P, D.L - 1, P.act.o_dout);
+        x.gain = P.w.final_norm;
+        if (res) x.resid = lt(P, D.L, P.act.o_h);
+      }
+      break;
+    case MPK_TASK_CHAIN_UP:
+      x.mode = X_NORM_EMBED;
+      x.gain = P.w.final_norm;
+      break;
+    default:  // MPK_TASK_CHAIN_DOWN
+      x.a = lt(P, 0, P.act.o_act);
+      break;
+  }
+  return x;
+}
+
+// Pre-norm values of 8 columns [k, k + 8) of sequence b.
+__device__ __forceinline__ void pre_values(const KernelParams& P,
+                                           const XSrc& x, int b, int K, int k,
+                                           float (&v)[8]) {
+  if (x.mode == X_NORM_EMBED) {
+    int tok = __ldg(P.step.tokens + b);
+    tok = min(max(tok, 0), P.dims.V - 1);
+    const uint4 e = __ldg(reinterpret_cast<const uint4*>(
+        P.w.embed + (int64_t)tok * K + k));
+    const uint32_t* pe = &e.x;
 #pragma unroll
-      for (int e = 0; e < DL; ++e) r[2 + lane * DL + e] = acc[hh][e];
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = bf_lo(pe[q]);
+      v[2 * q + 1] = bf_hi(pe[q]);
+    }
+  } else {
+    const uint4 va =
+        __ldcg(reinterpret_cast<const uint4*>(x.a + (int64_t)b * K + k));
+    const uint4 vc =
+        __ldcg(reinterpret_cast<const uint4*>(x.c + (int64_t)b * K + k));
+    const uint32_t* pa = &va.x;
+    const uint32_t* pc = &vc.x;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = round_bf(__fadd_rn(bf_lo(pa[q]), bf_lo(pc[q])));
+      v[2 * q + 1] = round_bf(__fadd_rn(bf_hi(pa[q]), bf_hi(pc[q])));
+    }
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+  return make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]),
+                    pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
+}
+// bf16((v * r) * w) for 8 columns (one rounding, the oracle's order).
+__device__ __forceinline__ uint4 norm8(const float (&v)[8], float r,
+                                       uint4 wv) {
+  const uint32_t* pw = &wv.x;
+  float o[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    o[2 * q] = __fmul_rn(__fmul_rn(v[2 * q], r), bf_lo(pw[q]));
+    o[2 * q + 1] = __fmul_rn(__fmul_rn(v[2 * q + 1], r), bf_hi(pw[q]));
+  }
+  return pack8(o);
+}
+__device__ __forceinline__ float rms_factor(float ss, int K, float eps) {
+  return 1.0f / sqrtf(ss / (float)K + eps);
+}
+
+// Batch 1: stage all K columns of x into S.xs.
+__device__ void stage_x_b1(const KernelParams& P, const Smem& S,
+                           const TaskDesc& t, const Gemv& g) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const XSrc x = x_source(P, t);
+  const int K = g.K, nch = K >> 3;
+  uint4* xs = reinterpret_cast<uint4*>(S.xs);
+  if (x.mode == X_PLAIN) {
+    for (int ch = tid; ch < nch; ch += kConsumers)
+      xs[ch] = __ldcg(reinterpret_cast<const uint4*>(x.a) + ch);
+    consumer_sync();
+    return;
+  }
+  constexpr int kMaxChunks = 4;  // K <= 8192 for normed operators
+  float v[kMaxChunks][8];
+  uint4 wv[kMaxChunks];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int ch = tid + k * kConsumers;
+    if (ch < nch) {
+      wv[k] = __ldg(reinterpret_cast<const uint4*>(x.gain) + ch);
+      pre_values(P, x, 0, K, ch * 8, v[k]);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ss = fmaf(v[k][q], v[k][q], ss);
+    }
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) S.scratch[warp] = ss;
+  consumer_sync();
+  float tot = 0.f;
+#pragma unroll
+  for (int q = 0; q < kConsumerWarps; ++q) tot += S.scratch[q];
+  const float r = rms_factor(tot, K, P.dims.eps);
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int ch = tid + k * kConsumers;
+    if (ch < nch) {
+      xs[ch] = norm8(v[k], r, wv[k]);
+      if (x.resid) reinterpret_cast<uint4*>(x.resid)[ch] = pack8(v[k]);
     }
   }
   consumer_sync();
-  float* out = reinterpret_cast<float*>(layer_base(P, l) + P.act.o_opart) +
-               (((int64_t)(b * D.Hkv + g) * D.C + t.c) * grp) * rec;
-  for (int o = threadIdx.x; o < grp * d; o += kConsumers) {
-    const int hh = o / d, i = o % d;
+}
+
+// Batch > 1, norm modes: the RMS factor of every sequence into
+// S.scratch[32 + b] (one warp per sequence); tile 0 stores the residual.
+__device__ void norm_stats(const KernelParams& P, const Smem& S,
+                           const TaskDesc& t, const Gemv& g) {
+  const XSrc x = x_source(P, t);
+  if (x.mode == X_PLAIN) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int K = g.K, nch = K >> 3;
+  for (int b = warp; b < P.dims.B; b += kConsumerWarps) {
+    float ss = 0.f;
+    for (int ch = lane; ch < nch; ch += 32) {
+      float v[8];
+      pre_values(P, x, b, K, ch * 8, v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
+      if (x.resid)
+        reinterpret_cast<uint4*>(x.resid + (int64_t)b * K)[ch] = pack8(v);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) S.scratch[32 + b] = rms_factor(ss, K, P.dims.eps);
+  }
+  consumer_sync();
+}
+
+// Batch > 1: stage column segment s of every sequence into S.xs, row b at
+// b * kPagePitch bytes; columns up to the next multiple of 16 are zeroed.
+__device__ void stage_x_seg(const KernelParams& P, const Smem& S,
+                            const TaskDesc& t, const Gemv& g, int s) {
+  const XSrc x = x_source(P, t);
+  const int B = P.dims.B, K = g.K;
+  const int c0 = s * kSegCols, cols = min(kSegCols, K - c0);
+  const int nch = cols >> 3, nch16 = ((cols + 15) >> 4) << 1;
+  consumer_sync();   // every warp is done with the previous segment
+  for (int idx = threadIdx.x; idx < B * nch16; idx += kConsumers) {
+    const int b = idx / nch16, ch = idx - b * nch16;
+    uint4* dst = reinterpret_cast<uint4*>(
+        reinterpret_cast<uint8_t*>(S.xs) + (size_t)b * kPagePitch) + ch;
+    if (ch >= nch) {
+      *dst = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const int k = c0 + ch * 8;
+    if (x.mode == X_PLAIN) {
+      *dst = __ldcg(reinterpret_cast<const uint4*>(x.a + (int64_t)b * K + k));
+    } else {
+      float v[8];
+      pre_values(P, x, b, K, k, v);
+      *dst = norm8(v, S.scratch[32 + b],
+                   __ldg(reinterpret_cast<const uint4*>(x.gain + k)));
+    }
+  }
+  consumer_sync();
+}
+
+// ------------------------------------------------------------ epilogue
+// Row results are in S.res[b * RP + page row]; write the operator's output.
+__device__ void gemv_epilogue(const KernelParams& P, const Smem& S,
+                              const TaskDesc& t, const Gemv& g) {
+  const Dims& D = P.dims;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = D.B, R = g.rows, RP = g.ngroups * kPageRows;
+  const float* res = S.res;
+  const int l = g.layer;
+  for (int idx = tid; idx < B * R; idx += kConsumers) {
+    const int b = idx / R, o = idx - b * R;
+    const int orow = g.row0 + o;
+    if (g.dual) {
+      const int j = o >> 2, i = o & 3;
+      const float gv = round_bf(res[b * RP + 8 * j + i]);
+      const float uv = round_bf(res[b * RP + 8 * j + 4 + i]);
+      lt(P, l, P.act.o_act)[(int64_t)b * g.N + orow] =
+          f2bf(__fmul_rn(silu_f(gv), uv));
+      continue;
+    }
+    const float v = res[b * RP + o];
+    switch (g.kind) {
+      case MPK_TASK_LM_HEAD:
+        P.step.logits[(int64_t)b * g.N + orow] = v;
+        break;
+      case MPK_TASK_CHAIN_UP:
+        lt(P, 0, P.act.o_act)[(int64_t)b * g.N + orow] =
+            f2bf(silu_f(round_bf(v)));
+        break;
+      case MPK_TASK_QKV:
+        lt(P, l, P.act.o_qkv)[(int64_t)b * g.N + orow] = f2bf(v);
+        break;
+      case MPK_TASK_O:
+        lt(P, l, P.act.o_o)[(int64_t)b * g.N + orow] = f2bf(v);
+        break;
+      case MPK_TASK_DOWN:
+        lt(P, l, P.act.o_dout)[(int64_t)b * g.N + orow] = f2bf(v);
+        break;
+      default:  // MPK_TASK_CHAIN_DOWN
+        reinterpret_cast<uint16_t*>(global_base(P) +
+                                    P.act.g_z)[(int64_t)b * g.N + orow] =
+            f2bf(v);
+        break;
+    }
+  }
+  if (g.kind != MPK_TASK_LM_HEAD) return;
+  // tile argmax (lowest index among equal maxima)
+  float2* am = reinterpret_cast<float2*>(global_base(P) + P.act.g_amax);
+  if (B == 1) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int o = tid; o < R; o += kConsumers)
+      if (better(res[o], g.row0 + o, bv, bi)) {
+        bv = res[o];
+        bi = g.row0 + o;
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, bv, off);
+      const int oi = __shfl_xor_sync(kFull, bi, off);
+      if (better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      S.scratch[64 + warp] = bv;
+      S.scratch[80 + warp] = __int_as_float(bi);
+    }
+    consumer_sync();
+    if (tid == 0) {
+      for (int w = 1; w < kConsumerWarps; ++w) {
+        const float ov = S.scratch[64 + w];
+        const int oi = __float_as_int(S.scratch[80 + w]);
+        if (better(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      am[t.tile] = make_float2(bv, __int_as_float(bi));
+    }
+    return;
+  }
+  for (int b = warp; b < B; b += kConsumerWarps) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int o = lane; o < R; o += 32)
+      if (better(res[b * RP + o], g.row0 + o, bv, bi)) {
+        bv = res[b * RP + o];
+        bi = g.row0 + o;
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, bv, off);
+      const int oi = __shfl_xor_sync(kFull, bi, off);
+      if (better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0)
+      am[(int64_t)b * D.n_lm_tiles + t.tile] =
+          make_float2(bv, __int_as_float(bi));
+  }
+}
+
+// ------------------------------------------------------------ MatMul bodies
+// Batch 1: warp w owns row w of every page; each lane reads 16-byte column
+// chunks lane, lane + 32, ... of that row and of x, four partial sums per
+// lane, one warp reduction per row.
+__device__ void gemv_b1(const KernelParams& P, const Smem& S,
+                        const TaskDesc& t, const Gemv& g, Ring& ring,
+                        uint64_t deadline) {
+  stage_x_b1(P, S, t, g);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int j = 0; j < g.ngroups; ++j) {
+    bool valid;
+    page_wrow(g, j, warp, valid);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (int s = 0; s < g.nsegs; ++s) {
+      const bool have = wait_full(P, S, ring, deadline);
+      if (have && valid) {
+        const int c0 = s * kSegCols, nch = min(kSegCols, g.K - c0) >> 3;
+        const uint4* row = reinterpret_cast<const uint4*>(
+            page_ptr(S, ring.slot) + warp * kPagePitch);
+        const uint4* xp = reinterpret_cast<const uint4*>(S.xs + c0);
+        if (nch == kSegCols / 8) {
+#pragma unroll
+          for (int k = 0; k < 8; k += 4) {
+            const int ch = lane + 32 * k;
+            a0 = dot8(row[ch], xp[ch], a0);
+            a1 = dot8(row[ch + 32], xp[ch + 32], a1);
+            a2 = dot8(row[ch + 64], xp[ch + 64], a2);
+            a3 = dot8(row[ch + 96], xp[ch + 96], a3);
+          }
+        } else {
+          for (int ch = lane; ch < nch; ch += 32) a0 = dot8(row[ch], xp[ch], a0);
+        }
+      }
+      release_page(S, ring, have);
+    }
+    const float acc = warp_sum((a0 + a1) + (a2 + a3));
+    if (lane == 0) S.res[j * kPageRows + warp] = acc;
+  }
+  consumer_sync();
+  gemv_epilogue(P, S, t, g);
+}
+
+// A tile with more row groups than a body keeps accumulators for cannot be
+// built by the host (its row cap); should one arrive anyway, its surplus
+// pages are consumed unread and the step reports MPK_ERR_UNSUPPORTED, so the
+// ring stays in step with the producer.
+__device__ void skip_extra_groups(const KernelParams& P, const Smem& S,
+                                  const Gemv& g, int kept, Ring& ring,
+                                  uint64_t deadline) {
+  if (g.ngroups <= kept) return;
+  if (threadIdx.x == 0) raise_error(P, MPK_ERR_UNSUPPORTED);
+  for (int j = kept; j < g.ngroups; ++j)
+    release_page(S, ring, wait_full(P, S, ring, deadline));
+}
+
+// Batch 2..7 on CUDA cores: column segments outer; warp w owns row w of
+// every page; up to 8 row groups per tile.
+template <int NB>
+__device__ void gemv_cc(const KernelParams& P, const Smem& S,
+                        const TaskDesc& t, const Gemv& g, Ring& ring,
+                        uint64_t deadline) {
+  constexpr int kMaxGroups = 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int B = P.dims.B, RP = g.ngroups * kPageRows;
+  norm_stats(P, S, t, g);
+  float acc[kMaxGroups][NB];
+#pragma unroll
+  for (int j = 0; j < kMaxGroups; ++j)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[j][b] = 0.f;
+  for (int s = 0; s < g.nsegs; ++s) {
+    stage_x_seg(P, S, t, g, s);
+    const int nch = min(kSegCols, g.K - s * kSegCols) >> 3;
+#pragma unroll
+    for (int j = 0; j < kMaxGroups; ++j) {
+      if (j < g.ngroups) {
+        bool valid;
+        page_wrow(g, j, warp, valid);
+        const bool have = wait_full(P, S, ring, deadline);
+        if (have && valid) {
+          const uint4* row = reinterpret_cast<const uint4*>(
+              page_ptr(S, ring.slot) + warp * kPagePitch);
+          for (int ch = lane; ch < nch; ch += 32) {
+            const uint4 wv = row[ch];
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+              if (b < B)
+                acc[j][b] = dot8(wv,
+                                 reinterpret_cast<const uint4*>(
+                                     reinterpret_cast<const uint8_t*>(S.xs) +
+                                     (size_t)b * kPagePitch)[ch],
+                                 acc[j][b]);
+          }
+        }
+        release_page(S, ring, have);
+      }
+    }
+    skip_extra_groups(P, S, g, kMaxGroups, ring, deadline);
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxGroups; ++j)
+    if (j < g.ngroups)
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+        if (b < B) {
+          const float v = warp_sum(acc[j][b]);
+          if (lane == 0) S.res[b * RP + j * kPageRows + warp] = v;
+        }
+  consumer_sync();
+  gemv_epilogue(P, S, t, g);
+}
+
+// Batch >= 8 on tensor cores: mma.sync m16n8k16 with the sequences as M
+// (rows >= batch repeat the last sequence and are discarded) and the page's
+// 8 weight rows as N.  Column segments outer; warp w owns row groups
+// j = w and j = w + 8 (at most 16 groups per tile), so no cross-warp
+// reduction is needed.
+__device__ void gemv_mma(const KernelParams& P, const Smem& S,
+                         const TaskDesc& t, const Gemv& g, Ring& ring,
+                         uint64_t deadline) {
+  constexpr int kMaxGroups = 16;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int B = P.dims.B, RP = g.ngroups * kPageRows;
+  norm_stats(P, S, t, g);
+  float acc[2][2][4];
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[a][c][e] = 0.f;
+  // ldmatrix row addresses: A = x rows (sequences), B = page rows
+  const int arow = min((lane & 7) + ((lane >> 3) & 1) * 8, B - 1);
+  const uint32_t a_base = smem_addr(S.xs) + arow * kPagePitch +
+                          ((lane >> 4) * 8) * 2;
+  const uint32_t b_off = (lane & 7) * kPagePitch + ((lane >> 3) * 8) * 2;
+  const int kq = (lane & 3) * 2;   // this lane's k within an 8-column block
+  for (int s = 0; s < g.nsegs; ++s) {
+    stage_x_seg(P, S, t, g, s);
+    const int cols = min(kSegCols, g.K - s * kSegCols);
+    const int ksteps = (cols + 15) >> 4;
+#pragma unroll
+    for (int j = 0; j < kMaxGroups; ++j) {
+      if (j < g.ngroups) {
+        const bool have = wait_full(P, S, ring, deadline);
+        if (have && (j & 7) == warp) {
+          const uint32_t pb = smem_addr(page_ptr(S, ring.slot)) + b_off;
+          float (&c0)[4] = acc[j >> 3][0];
+          float (&c1)[4] = acc[j >> 3][1];
+          for (int ks = 0; ks < ksteps; ks += 2) {
+            uint32_t b0, b1, b2, b3, x0, x1, x2, x3;
+            ldsm_x4(pb + ks * 32, b0, b1, b2, b3);
+            ldsm_x4(a_base + ks * 32, x0, x1, x2, x3);
+            const int kb = ks * 16 + kq;
+            if (kb >= cols) b0 = 0u;
+            if (kb + 8 >= cols) b1 = 0u;
+            mma_16816(c0, x0, x1, x2, x3, b0, b1);
+            if (ks + 1 < ksteps) {
+              ldsm_x4(a_base + ks * 32 + 32, x0, x1, x2, x3);
+              if (kb + 16 >= cols) b2 = 0u;
+              if (kb + 24 >= cols) b3 = 0u;
+              mma_16816(c1, x0, x1, x2, x3, b2, b3);
+            }
+          }
+        }
+        release_page(S, ring, have);
+      }
+    }
+    skip_extra_groups(P, S, g, kMaxGroups, ring, deadline);
+  }
+  // D fragment: rows (sequences) lane/4 and lane/4 + 8, columns (page rows)
+  // (lane % 4) * 2 and + 1
+  const int bq = lane >> 2, nq = (lane & 3) * 2;
+#pragma unroll
+  for (int a = 0; a < 2; ++a) {
+    const int j = warp + 8 * a;
+    if (j < g.ngroups) {
+      const float d0 = acc[a][0][0] + acc[a][1][0];
+      const float d1 = acc[a][0][1] + acc[a][1][1];
+      const float d2 = acc[a][0][2] + acc[a][1][2];
+      const float d3 = acc[a][0][3] + acc[a][1][3];
+      const int pr = j * kPageRows + nq;
+      if (bq < B) {
+        S.res[bq * RP + pr] = d0;
+        S.res[bq * RP + pr + 1] = d1;
+      }
+      if (bq + 8 < B) {
+        S.res[(bq + 8) * RP + pr] = d2;
+        S.res[(bq + 8) * RP + pr + 1] = d3;
+      }
+    }
+  }
+  consumer_sync();
+  gemv_epilogue(P, S, t, g);
+}
+
+// ------------------------------------------------------------ attention
+// q/k RMSNorm (optional) and rotate-half RoPE of one head: lane l holds
+// dims [l*DL, l*DL + DL); the partner of dim i < d/2 is i + d/2, held by
+// lane l ^ 16.  Values are rounded to bf16 after the norm and after RoPE.
+template <int DL>
+__device__ __forceinline__ void rope_head(const KernelParams& P,
+                                          const uint16_t* src,
+                                          const uint16_t* nw, const float* cs,
+                                          bool rot, float (&x)[DL]) {
+  const Dims& D = P.dims;
+  const int lane = threadIdx.x & 31, d = DL * 32;
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < DL; ++e) {
+    x[e] = bf2f(__ldcg(src + lane * DL + e));
+    ss = fmaf(x[e], x[e], ss);
+  }
+  if (!rot) return;
+  if (nw) {
+    ss = warp_sum(ss);
+    const float r = 1.0f / sqrtf(ss / (float)d + D.eps);
+#pragma unroll
+    for (int e = 0; e < DL; ++e)
+      x[e] = round_bf(__fmul_rn(__fmul_rn(x[e], r),
+                                bf2f(__ldg(nw + lane * DL + e))));
+  }
+  const bool lo = lane < 16;
+#pragma unroll
+  for (int e = 0; e < DL; ++e) {
+    const float other = __shfl_xor_sync(kFull, x[e], 16);
+    const int i = (lane & 15) * DL + e;
+    const float c = __ldg(cs + 2 * i), s = __ldg(cs + 2 * i + 1);
+    const float y = lo ? __fsub_rn(__fmul_rn(x[e], c), __fmul_rn(other, s))
+                       : __fadd_rn(__fmul_rn(x[e], c), __fmul_rn(other, s));
+    x[e] = round_bf(y);
+  }
+}
+
+// Sum 32 per-lane values across the warp so that lane j ends with the total
+// of value j (a transpose-reduce: 31 shuffles for 32 sums).
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = up ? v[i] : v[i + o];
+      const float keep = up ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFull, send, o);
+    }
+  }
+  return v[0];
+}
+
+__device__ __forceinline__ void load_row(const uint16_t* p, int DLc,
+                                         float* out) {
+  if (DLc == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    out[0] = bf_lo(u.x);
+    out[1] = bf_hi(u.x);
+    out[2] = bf_lo(u.y);
+    out[3] = bf_hi(u.y);
+  } else if (DLc == 2) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    out[0] = bf_lo(u);
+    out[1] = bf_hi(u);
+  } else {
+    out[0] = bf2f(*p);
+  }
+}
+__device__ __forceinline__ void load_row_cg(const uint16_t* p, int DLc,
+                                            float* out) {
+  if (DLc == 4) {
+    const uint2 u = __ldcg(reinterpret_cast<const uint2*>(p));
+    out[0] = bf_lo(u.x);
+    out[1] = bf_hi(u.x);
+    out[2] = bf_lo(u.y);
+    out[3] = bf_hi(u.y);
+  } else if (DLc == 2) {
+    const uint32_t u = __ldcg(reinterpret_cast<const unsigned int*>(p));
+    out[0] = bf_lo(u);
+    out[1] = bf_hi(u);
+  } else {
+    out[0] = bf2f(__ldcg(p));
+  }
+}
+
+// Row `tok` of the K (or V) chunk, this lane's DL values: from the ring
+// page (AOT) or the paged cache (JIT); zero past the chunk.
+template <int DL>
+__device__ __forceinline__ void attn_row(const KernelParams& P, bool pre,
+                                         const uint8_t* page,
+                                         const uint16_t* pool, int tok,
+                                         int t0, int t1, int64_t layer_elems,
+                                         int64_t head_elems, const int32_t* pt,
+                                         float (&out)[DL]) {
+  const int lane = threadIdx.x & 31, d = DL * 32;
+#pragma unroll
+  for (int e = 0; e < DL; ++e) out[e] = 0.f;
+  if (tok >= t1) return;
+  if (pre) {
+    load_row(reinterpret_cast<const uint16_t*>(page) + (size_t)(tok - t0) * d +
+                 lane * DL,
+             DL, out);
+    return;
+  }
+  const Dims& D = P.dims;
+  const int page_id = __ldg(pt + tok / D.page_size);
+  if (page_id >= 0 && page_id < P.step.num_pages) {
+    load_row_cg(pool + layer_elems + (int64_t)page_id * D.Hkv * head_elems +
+                    (int64_t)(tok % D.page_size) * d + lane * DL,
+                DL, out);
+  } else if (lane == 0) {
+    raise_error(P, MPK_ERR_KV_PAGE);
+  }
+}
+
+// One KV chunk of (sequence b, KV head g): tokens [t0, t1) of the
+// n = seq_len + 1 positions.  Prologue: the group's queries (and, for the
+// chunk holding the new token, its key and value) get RMSNorm + RoPE; the
+// new K/V are appended to the paged cache.  Body: each warp runs an online
+// softmax over blocks of 32/GRP tokens for all GRP query heads (lane j of a
+// block scores token j/GRP against head j%GRP).  The warps merge into one
+// (m, l, acc) partial per head; the last chunk of (b, g) to finish merges
+// the C partials (log-sum-exp) into the bf16 attention output.  AOT tasks
+// read their cached tokens from two ring pages the producer filled ahead of
+// time; JIT tasks read the paged cache directly.
+template <int DL, int GRP>
+__device__ void attn_body(const KernelParams& P, const Smem& S,
+                          const TaskDesc& t, Ring& ring, uint64_t deadline) {
+  constexpr int d = DL * 32, TB = 32 / GRP;
+  const Dims& D = P.dims;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = t.b, g = t.g, l = t.layer, C = D.C;
+  const bool pre = t.launch == MPK_LAUNCH_AOT;
+  const int pos = __ldcg(P.step.seq_lens + b);
+  const int n = pos + 1;
+  float* qf = reinterpret_cast<float*>(S.xs);       // [GRP][d]
+  float* knew = qf + GRP * d;                        // [d]
+  float* vnew = knew + d;                            // [d]
+  float* wbuf = vnew + d;                            // [8][GRP][2 + d]
+  bool have_k = true, have_v = true;
+  uint8_t *kpage = nullptr, *vpage = nullptr;
+  Ring kr = ring;
+  if (pre) {
+    have_k = wait_full(P, S, ring, deadline);
+    kpage = page_ptr(S, ring.slot);
+    ring.advance(S.n_pages);
+    have_v = wait_full(P, S, ring, deadline);
+    vpage = page_ptr(S, ring.slot);
+    ring.advance(S.n_pages);
+  }
+  int t0 = 0, t1 = 0;
+  int page_new = -1;
+  bool ok = pos >= 0 && n <= D.max_ctx;
+  if (ok) {
+    chunk_range(t.c, n, C, t0, t1);
+    if (pre) t1 = min(t1, t0 + kAttnMaxTokens);
+    const int pidx = pos / D.page_size;
+    if (pidx < D.max_pages)
+      page_new = __ldg(P.step.page_table + (int64_t)b * D.max_pages + pidx);
+    ok = page_new >= 0 && page_new < P.step.num_pages;
+  }
+  if (!ok) {
+    if (tid == 0) raise_error(P, MPK_ERR_KV_PAGE);
+    t0 = t1 = 0;
+  }
+  const bool has_new = ok && t1 == n && t1 > t0;
+  // ---- prologue: queries (and the new key/value) into shared memory
+  {
+    const uint16_t* qkv = lt(P, l, P.act.o_qkv) +
+                          (int64_t)b * (D.Hq + 2 * D.Hkv) * d;
+    const float* cs = P.w.rope_cs + (int64_t)(ok ? pos : 0) * (d / 2) * 2;
+    const int64_t slot =
+        ((((int64_t)l * P.step.num_pages + max(page_new, 0)) * D.Hkv + g) *
+             D.page_size +
+         (ok ? pos % D.page_size : 0)) *
+        d;
+    for (int hh = warp; hh < GRP + 2; hh += kConsumerWarps) {
+      if (hh >= GRP && !has_new) continue;
+      const uint16_t* src;
+      const uint16_t* nw = nullptr;
+      if (hh < GRP) {
+        src = qkv + (int64_t)(g * GRP + hh) * d;
+        if (D.qk_norm) nw = layer_w(P, l, MPK_W_QNORM);
+      } else if (hh == GRP) {
+        src = qkv + (int64_t)(D.Hq + g) * d;
+        if (D.qk_norm) nw = layer_w(P, l, MPK_W_KNORM);
+      } else {
+        src = qkv + (int64_t)(D.Hq + D.Hkv + g) * d;
+      }
+      float x[DL];
+      rope_head<DL>(P, src, nw, cs, hh <= GRP, x);
+      float* dst = hh < GRP ? qf + hh * d : (hh == GRP ? knew : vnew);
+#pragma unroll
+      for (int e = 0; e < DL; ++e) dst[lane * DL + e] = x[e];
+      if (hh >= GRP) {
+        uint16_t* cache = (hh == GRP ? P.step.k_pool : P.step.v_pool) + slot;
+        uint16_t* pg = pre ? reinterpret_cast<uint16_t*>(
+                                 (hh == GRP ? kpage : vpage)) +
+                                 (size_t)(pos - t0) * d
+                           : nullptr;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) {
+          const uint16_t u = f2bf(x[e]);
+          cache[lane * DL + e] = u;
+          if (pg) pg[lane * DL + e] = u;
+        }
+      }
+    }
+    if (!pre) __threadfence();   // the new K/V row is read back below
+    consumer_sync();
+  }
+  float qr[GRP][DL];
+#pragma unroll
+  for (int h = 0; h < GRP; ++h)
+#pragma unroll
+    for (int e = 0; e < DL; ++e) qr[h][e] = qf[h * d + lane * DL + e];
+  // ---- online softmax over this warp's token blocks
+  const int my_h = lane % GRP;
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[GRP][DL];
+#pragma unroll
+  for (int h = 0; h < GRP; ++h)
+#pragma unroll
+    for (int e = 0; e < DL; ++e) acc[h][e] = 0.f;
+  const int64_t head_elems = (int64_t)D.page_size * d;
+  const int64_t layer_elems =
+      (int64_t)l * P.step.num_pages * D.Hkv * head_elems +
+      (int64_t)g * head_elems;
+  const int32_t* pt = P.step.page_table + (int64_t)b * D.max_pages;
+  const int ntok = t1 - t0;
+  const int nblk = (ntok + TB - 1) / TB;
+  for (int blk = warp; blk < nblk; blk += kConsumerWarps) {
+    // scores: one K row at a time
+    float sv[32];
+#pragma unroll
+    for (int tb = 0; tb < TB; ++tb) {
+      const int tok = t0 + blk * TB + tb;
+      float kf[DL];
+      attn_row(P, pre, kpage, P.step.k_pool, tok, t0, t1, layer_elems,
+               head_elems, pt, kf);
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) s = fmaf(qr[h][e], kf[e], s);
+        sv[tb * GRP + h] = s;
+      }
+    }
+    float s = reduce_scatter32(sv) * D.attn_scale;
+    const int my_tok = t0 + blk * TB + lane / GRP;
+    if (my_tok >= t1) s = -INFINITY;
+    float mb = s;
+#pragma unroll
+    for (int o = GRP; o < 32; o <<= 1)
+      mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+    const float m_new = fmaxf(m_run, mb);   // finite: the block's token 0 is
+                                            // always valid
+    const float corr = (m_run == -INFINITY) ? 0.f : expf(m_run - m_new);
+    const float p = (s == -INFINITY) ? 0.f : expf(s - m_new);
+    float lb = p;
+#pragma unroll
+    for (int o = GRP; o < 32; o <<= 1) lb += __shfl_xor_sync(kFull, lb, o);
+    l_run = l_run * corr + lb;
+    m_run = m_new;
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+      const float ch = __shfl_sync(kFull, corr, h);
+#pragma unroll
+      for (int e = 0; e < DL; ++e) acc[h][e] *= ch;
+    }
+#pragma unroll
+    for (int tb = 0; tb < TB; ++tb) {
+      const int tok = t0 + blk * TB + tb;
+      float vf[DL];
+      attn_row(P, pre, vpage, P.step.v_pool, tok, t0, t1, layer_elems,
+               head_elems, pt, vf);
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        const float pth = __shfl_sync(kFull, p, tb * GRP + h);
+#pragma unroll
+        for (int e = 0; e < DL; ++e) acc[h][e] = fmaf(pth, vf[e], acc[h][e]);
+      }
+    }
+  }
+  if (pre) {
+    // the pages were written through the generic proxy (new token): order
+    // that before the producer's next bulk copy into them
+    fence_proxy_async_smem();
+    release_page(S, kr, have_k);
+    release_page(S, kr, have_v);
+  }
+  // ---- merge the 8 warps into this chunk's partial
+  constexpr int rec = 2 + d;
+#pragma unroll
+  for (int h = 0; h < GRP; ++h) {
+    float* r = wbuf + (warp * GRP + h) * rec;
+    const float mh = __shfl_sync(kFull, m_run, h);
+    const float lh = __shfl_sync(kFull, l_run, h);
+    if (lane == 0) {
+      r[0] = mh;
+      r[1] = lh;
+    }
+#pragma unroll
+    for (int e = 0; e < DL; ++e) r[2 + lane * DL + e] = acc[h][e];
+  }
+  consumer_sync();
+  float* part = lt<float>(P, l, P.act.o_opart) +
+                (((int64_t)(b * D.Hkv + g) * C) * GRP) * rec;
+  float* mine = part + (int64_t)t.c * GRP * rec;
+  for (int o = tid; o < GRP * d; o += kConsumers) {
+    const int h = o / d, i = o - h * d;
     float M = -INFINITY;
+#pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w)
-      M = fmaxf(M, wbuf[((int64_t)w * grp + hh) * rec]);
-    float L = 0.f, A = 0.f;
+      M = fmaxf(M, wbuf[(w * GRP + h) * rec]);
+    float Ls = 0.f, A = 0.f;
     if (M != -INFINITY) {
+#pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float* r = wbuf + ((int64_t)w * grp + hh) * rec;
+        const float* r = wbuf + (w * GRP + h) * rec;
         const float sc = (r[0] == -INFINITY) ? 0.f : expf(r[0] - M);
-        L = fmaf(r[1], sc, L);
+        Ls = fmaf(r[1], sc, Ls);
         A = fmaf(r[2 + i], sc, A);
       }
     }
-    out[(int64_t)hh * rec + 2 + i] = A;
+    mine[h * rec + 2 + i] = A;
     if (i == 0) {
-      out[(int64_t)hh * rec] = M;
-      out[(int64_t)hh * rec + 1] = L;
+      mine[h * rec] = M;
+      mine[h * rec + 1] = Ls;
     }
   }
+  __threadfence();
   consumer_sync();
+  // ---- the last chunk of (b, g) to finish merges all C partials
+  if (tid == 0) {
+    uint32_t* cnt = P.graph.merge_cnt + ((int64_t)l * D.B + b) * D.Hkv + g;
+    const uint32_t old = atom_acq_rel_add(cnt, 1u);
+    const int last = (old + 1u == (uint32_t)C) ? 1 : 0;
+    if (last) *reinterpret_cast<volatile uint32_t*>(cnt) = 0u;
+    S.ctrl[4] = last;
+  }
+  consumer_sync();
+  if (!S.ctrl[4]) return;
+  uint16_t* out = lt(P, l, P.act.o_attn) + (int64_t)b * D.Hq * d +
+                  (int64_t)g * GRP * d;
+  for (int o = tid; o < GRP * d; o += kConsumers) {
+    const int h = o / d, i = o - h * d;
+    float M = -INFINITY;
+    for (int c = 0; c < C; ++c)
+      M = fmaxf(M, __ldcg(part + ((int64_t)c * GRP + h) * rec));
+    float Ls = 0.f, A = 0.f;
+    for (int c = 0; c < C; ++c) {
+      const float* r = part + ((int64_t)c * GRP + h) * rec;
+      const float mc = __ldcg(r);
+      const float sc = (mc == -INFINITY) ? 0.f : expf(mc - M);
+      Ls = fmaf(__ldcg(r + 1), sc, Ls);
+      A = fmaf(__ldcg(r + 2 + i), sc, A);
+    }
+    out[o] = f2bf(A / Ls);
+  }
 }
 
 __device__ void task_attn(const KernelParams& P, const Smem& S,
-                          const TaskDesc& t) {
+                          const TaskDesc& t, Ring& ring, uint64_t deadline) {
   const int grp = P.dims.Hq / P.dims.Hkv;
   const int dl = P.dims.d / 32;
-  if (grp <= 4) {
-    switch (dl) {
-      case 1: attn_body<1, 4>(P, S, t); break;
-      case 2: attn_body<2, 4>(P, S, t); break;
-      case 3: attn_body<3, 4>(P, S, t); break;
-      default: attn_body<4, 4>(P, S, t); break;
-    }
-  } else if (grp <= 8) {
-    switch (dl) {
-      case 1: attn_body<1, 8>(P, S, t); break;
-      case 2: attn_body<2, 8>(P, S, t); break;
-      case 3: attn_body<3, 8>(P, S, t); break;
-      default: attn_body<4, 8>(P, S, t); break;
-    }
-  } else {
-    switch (dl) {
-      case 1: attn_body<1, 16>(P, S, t); break;
-      default: attn_body<2, 16>(P, S, t); break;
-    }
+#define MPK_ATTN_CASE(G)                                   \
+  if (grp == G) {                                          \
+    if (dl == 4) attn_body<4, G>(P, S, t, ring, deadline); \
+    else if (dl == 2) attn_body<2, G>(P, S, t, ring, deadline); \
+    else attn_body<1, G>(P, S, t, ring, deadline);         \
+    return;                                                \
   }
-}
-
-// Log-sum-exp merge of the C chunk partials of (b, g) -> bf16 attention
-// output of the group's query heads.
-__device__ void task_merge(const KernelParams& P, const Smem& S,
-                           const TaskDesc& t) {
-  const Dims& D = P.dims;
-  const int b = t.b, g = t.g, l = t.layer, d = D.d;
-  const int grp = D.Hq / D.Hkv, rec = 2 + d;
-  const float* part = reinterpret_cast<const float*>(layer_base(P, l) +
-                                                     P.act.o_opart) +
-                      ((int64_t)(b * D.Hkv + g) * D.C * grp) * rec;
-  uint16_t* out = reinterpret_cast<uint16_t*>(layer_base(P, l) + P.act.o_attn) +
-                  (int64_t)b * D.Hq * d + (int64_t)g * grp * d;
-  for (int o = threadIdx.x; o < grp * d; o += kConsumers) {
-    const int hh = o / d, i = o % d;
-    float M = -INFINITY;
-    for (int c = 0; c < D.C; ++c)
-      M = fmaxf(M, __ldcg(part + ((int64_t)c * grp + hh) * rec));
-    float L = 0.f, A = 0.f;
-    for (int c = 0; c < D.C; ++c) {
-      const float* r = part + ((int64_t)c * grp + hh) * rec;
-      const float mc = __ldcg(r);
-      const float sc = (mc == -INFINITY) ? 0.f : expf(mc - M);
-      L = fmaf(__ldcg(r + 1), sc, L);
-      A = fmaf(__ldcg(r + 2 + i), sc, A);
-    }
-    out[o] = f2bf(A / L);
-  }
+  MPK_ATTN_CASE(1)
+  MPK_ATTN_CASE(2)
+  MPK_ATTN_CASE(4)
+  MPK_ATTN_CASE(8)
+#undef MPK_ATTN_CASE
+  if (threadIdx.x == 0) raise_error(P, MPK_ERR_UNSUPPORTED);
 }
 
 // Greedy argmax over the lm_head tiles' (max, index) pairs; lowest index
 // among equal maxima.  Also advances seq_lens (decoder mode).
-__device__ void task_argmax(const KernelParams& P, const Smem& S,
-                            const TaskDesc& t) {
+__device__ void task_argmax(const KernelParams& P, const Smem& S) {
   const Dims& D = P.dims;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float2* am = reinterpret_cast<const float2*>(global_base(P) +
-                                                     P.act.g_amax);
+  const float2* am =
+      reinterpret_cast<const float2*>(global_base(P) + P.act.g_amax);
   for (int b = 0; b < D.B; ++b) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     for (int j = tid; j < D.n_lm_tiles; j += kConsumers) {
       const float2 e = __ldcg(am + (int64_t)b * D.n_lm_tiles + j);
-      const int idx = __float_as_int(e.y);
-      if (e.x > bv || (e.x == bv && idx < bi)) {
+      if (better(e.x, __float_as_int(e.y), bv, bi)) {
         bv = e.x;
-        bi = idx;
+        bi = __float_as_int(e.y);
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
+      const float ov = __shfl_xor_sync(kFull, bv, o);
+      const int oi = __shfl_xor_sync(kFull, bi, o);
+      if (better(ov, oi, bv, bi)) {
         bv = ov;
         bi = oi;
       }
@@ -848,251 +1581,42 @@ __device__ void task_argmax(const KernelParams& P, const Smem& S,
       for (int w = 1; w < kConsumerWarps; ++w) {
         const float ov = S.scratch[w];
         const int oi = __float_as_int(S.scratch[16 + w]);
-        if (ov > bv || (ov == bv && oi < bi)) {
+        if (better(ov, oi, bv, bi)) {
           bv = ov;
           bi = oi;
         }
       }
       P.step.next_tokens[b] = (bi == 0x7fffffff) ? 0 : bi;
-      if (D.chain_ffn == 0) P.step.seq_lens[b] = __ldcg(P.step.seq_lens + b) + 1;
+      if (D.chain_ffn == 0)
+        P.step.seq_lens[b] = __ldcg(P.step.seq_lens + b) + 1;
     }
     consumer_sync();
-  }
-}
-
-// Bounded wait for a weight page.  On timeout or abort the thread records a
-// bail-out in shared memory and carries on without the page (the step's
-// result is void by then), so every consumer thread still reaches the same
-// barriers and the CTA leaves its loop together.
-__device__ __forceinline__ bool wait_page(const KernelParams& P, const Smem& S,
-                                          const Ring& ring,
-                                          uint64_t deadline) {
-  if (S.ctrl[2]) return false;
-  uint32_t spins = 0;
-  while (!mbar_try_wait(&S.full[ring.slot], ring.phase)) {
-    if ((++spins & 1023u) == 0u && (aborted(P) || globaltimer() > deadline)) {
-      if (!aborted(P)) raise_error(P, MPK_ERR_TIMEOUT);
-      S.ctrl[2] = 1;
-      return false;
-    }
-  }
-  return true;
-}
-
-// MatMul tile: out[b][row] = sum_k x[b][k] W[row][k] for the task's rows,
-// consuming the weight pages the producer streams.  Thread (gbox, r) owns
-// row r of column box gbox of every page of a row-block; the four column
-// boxes are summed at the end of the row-block.
-template <int NB>
-__device__ void task_gemv(const KernelParams& P, const Smem& S,
-                          const TaskDesc& t, Ring& ring, uint64_t deadline) {
-  const Dims& D = P.dims;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int B = D.B;
-  const Gemv g = gemv_geom(P, t);
-  const int n_pages = P.graph.n_pages;
-  // x staging: [B][XC] bf16, XC a multiple of the page width
-  const int XC = ((kXsBytes / 2 / B) / kPageCols) * kPageCols;
-  const int nrb = rb_count(g), nkp = kpages(g);
-  int loaded = -1;
-  float best_v[NB];
-  int best_i[NB];
-#pragma unroll
-  for (int bb = 0; bb < NB; ++bb) {
-    best_v[bb] = -INFINITY;
-    best_i[bb] = 0x7fffffff;
-  }
-  for (int rb = 0; rb < nrb; ++rb) {
-    const int len = rb_len(g, rb);
-    const int r8 = (len + kBoxRows - 1) / kBoxRows;
-    const int prow8 = g.dual ? 2 * r8 : r8;
-    const int prows = prow8 * kBoxRows;
-    const int gb = tid / prows, r = tid % prows;
-    const bool mapped = gb < 4;
-    float acc[NB];
-#pragma unroll
-    for (int bb = 0; bb < NB; ++bb) acc[bb] = 0.f;
-    for (int x0 = 0; x0 < g.K; x0 += XC) {
-      if (x0 != loaded) {
-        consumer_sync();
-        const int xw = min(XC, g.K - x0);
-        const int xpad = ((xw + 63) / 64) * 64;
-        for (int bb = 0; bb < B; ++bb) {
-          const uint16_t* src = g.src + (int64_t)bb * g.K + x0;
-          uint16_t* dst = S.xs + bb * XC;
-          for (int i = tid * 8; i < xpad; i += kConsumers * 8) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (i < xw) v = __ldcg(reinterpret_cast<const uint4*>(src + i));
-            *reinterpret_cast<uint4*>(dst + i) = v;
-          }
-        }
-        consumer_sync();
-        loaded = x0;
-      }
-      const int cb_end = min(nkp, (x0 + XC) / kPageCols);
-      for (int cb = x0 / kPageCols; cb < cb_end; ++cb) {
-        const int nbc = min(4, (g.K - cb * kPageCols + 63) / 64);
-        const bool have = wait_page(P, S, ring, deadline);
-        if (have && mapped && gb < nbc) {
-          const uint8_t* rowp = S.pages + (size_t)ring.slot * kPageBytes +
-                                ((size_t)(gb * prow8 + (r >> 3)) << 10) +
-                                ((r & 7) << 7);
-          const uint16_t* xp = S.xs + (cb * kPageCols - x0) + gb * 64;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 wv = *reinterpret_cast<const uint4*>(
-                rowp + ((j ^ (r & 7)) << 4));
-#pragma unroll
-            for (int bb = 0; bb < NB; ++bb) {
-              if (bb < B) {
-                const uint4 xv =
-                    *reinterpret_cast<const uint4*>(xp + bb * XC + j * 8);
-                acc[bb] = dot8(wv, xv, acc[bb]);
-              }
-            }
-          }
-        }
-        // a page that never arrived (aborted step) is not released, so the
-        // producer cannot refill a slot a copy may still be writing
-        if (__all_sync(0xffffffffu, have) && lane == 0)
-          mbar_arrive(&S.empty[ring.slot]);
-        __syncwarp();
-        ring.advance(n_pages);
-      }
-    }
-    // reduce the four column boxes of each page row
-    if (mapped) {
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb)
-        if (bb < B) S.red[((gb * prows) + r) * B + bb] = acc[bb];
-    }
-    consumer_sync();
-    const int out_rows = g.dual ? r8 * kBoxRows : prows;
-    if (tid < out_rows) {
-      const int orow = g.row0 + rb * g.rb_rows + tid;
-      const bool valid = tid < len;
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb) {
-        if (bb < B && valid) {
-          float v = 0.f, u = 0.f;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) v += S.red[((q * prows) + tid) * B + bb];
-          if (g.dual) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              u += S.red[((q * prows) + r8 * kBoxRows + tid) * B + bb];
-          }
-          switch (g.kind) {
-            case MPK_TASK_LM_HEAD: {
-              P.step.logits[(int64_t)bb * g.N + orow] = v;
-              if (v > best_v[bb] || (v == best_v[bb] && orow < best_i[bb])) {
-                best_v[bb] = v;
-                best_i[bb] = orow;
-              }
-              break;
-            }
-            case MPK_TASK_GATEUP: {
-              const float gv = round_bf(v), uv = round_bf(u);
-              uint16_t* o = reinterpret_cast<uint16_t*>(
-                  layer_base(P, g.layer) + P.act.o_act);
-              o[(int64_t)bb * g.N + orow] = f2bf(__fmul_rn(silu_f(gv), uv));
-              break;
-            }
-            case MPK_TASK_CHAIN_UP: {
-              uint16_t* o = reinterpret_cast<uint16_t*>(layer_base(P, 0) +
-                                                        P.act.o_act);
-              o[(int64_t)bb * g.N + orow] = f2bf(silu_f(round_bf(v)));
-              break;
-            }
-            default: {
-              uint16_t* o;
-              if (g.kind == MPK_TASK_QKV)
-                o = reinterpret_cast<uint16_t*>(layer_base(P, g.layer) + P.act.o_qkv);
-              else if (g.kind == MPK_TASK_O)
-                o = reinterpret_cast<uint16_t*>(layer_base(P, g.layer) + P.act.o_o);
-              else if (g.kind == MPK_TASK_DOWN)
-                o = reinterpret_cast<uint16_t*>(layer_base(P, g.layer) + P.act.o_dout);
-              else
-                o = reinterpret_cast<uint16_t*>(global_base(P) + P.act.g_z);
-              o[(int64_t)bb * g.N + orow] = f2bf(v);
-              break;
-            }
-          }
-        }
-      }
-    }
-    consumer_sync();
-  }
-  if (g.kind == MPK_TASK_LM_HEAD) {
-    // tile argmax over threads 0..63 (warps 0 and 1)
-    const int warp = tid >> 5;
-#pragma unroll
-    for (int bb = 0; bb < NB; ++bb) {
-      if (bb >= B) break;
-      float bv = best_v[bb];
-      int bi = best_i[bb];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if (lane == 0 && warp < 2) {
-        S.scratch[2 * warp] = bv;
-        S.scratch[2 * warp + 1] = __int_as_float(bi);
-      }
-      consumer_sync();
-      if (tid == 0) {
-        const float ov = S.scratch[2];
-        const int oi = __float_as_int(S.scratch[3]);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-        float2* am = reinterpret_cast<float2*>(global_base(P) + P.act.g_amax);
-        am[(int64_t)bb * D.n_lm_tiles + t.tile] =
-            make_float2(bv, __int_as_float(bi));
-      }
-      consumer_sync();
-    }
   }
 }
 
 __device__ void run_task(const KernelParams& P, const Smem& S,
                          const TaskDesc& t, Ring& ring, uint64_t deadline) {
+  if (is_gemv(t.kind)) {
+    const Gemv g = gemv_geom(P, t);
+    const int B = P.dims.B;
+    if (B == 1)
+      gemv_b1(P, S, t, g, ring, deadline);
+    else if (B <= 4)
+      gemv_cc<4>(P, S, t, g, ring, deadline);
+    else if (B < 8)
+      gemv_cc<8>(P, S, t, g, ring, deadline);
+    else
+      gemv_mma(P, S, t, g, ring, deadline);
+    return;
+  }
   switch (t.kind) {
-    case MPK_TASK_NORM1:
-    case MPK_TASK_NORM2:
-    case MPK_TASK_FINAL_NORM:
-    case MPK_TASK_CHAIN_NORM:
-      task_norm(P, S, t);
-      break;
-    case MPK_TASK_ROPE:
-      task_rope(P, S, t);
-      break;
     case MPK_TASK_ATTN:
-      task_attn(P, S, t);
-      break;
-    case MPK_TASK_MERGE:
-      task_merge(P, S, t);
+      task_attn(P, S, t, ring, deadline);
       break;
     case MPK_TASK_ARGMAX:
-      task_argmax(P, S, t);
+      task_argmax(P, S);
       break;
-    case MPK_TASK_EMPTY:
-      break;
-    default:
-      if (P.dims.B == 1)
-        task_gemv<1>(P, S, t, ring, deadline);
-      else if (P.dims.B <= 4)
-        task_gemv<4>(P, S, t, ring, deadline);
-      else if (P.dims.B <= 8)
-        task_gemv<8>(P, S, t, ring, deadline);
-      else
-        task_gemv<16>(P, S, t, ring, deadline);
+    default:  // MPK_TASK_EMPTY
       break;
   }
 }
@@ -1166,25 +1690,6 @@ __device__ __forceinline__ bool event_done(const KernelParams& P, int e) {
 }
 
 // ------------------------------------------------------------ roles
-__device__ void producer_role(const KernelParams& P, const Smem& S,
-                              const int32_t* list, int n, uint64_t deadline) {
-  uint32_t issued[16];
-  for (int i = 0; i < 16; ++i) issued[i] = 0;
-  Ring ring{0, 0};
-  const uint64_t policy = evict_first_policy();
-  for (int i = 0; i < n; ++i) {
-    const TaskDesc t = P.graph.tasks[list[i]];
-    if (!is_gemv(t.kind)) continue;
-    if (!produce_gemv(P, S, gemv_geom(P, t), ring, issued, deadline, policy)) {
-      drain_copies(P, S, issued);
-      return;
-    }
-  }
-  // the consumers wait for every page before leaving, so all copies have
-  // landed by the time the CTA exits unless the step aborted
-  if (aborted(P)) drain_copies(P, S, issued);
-}
-
 __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
                                  uint64_t deadline) {
   const DevGraph& G = P.graph;
@@ -1194,30 +1699,44 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
   uint32_t jit_head = 0;
   RingHdr* jh = G.jit_hdr + w;
   uint64_t* js = G.jit_slots + (size_t)w * G.jit_cap;
-  if (tid == 0) jit_head = ld_relaxed(&jh->head);
+  // The head AOT task's descriptor is prefetched into shared memory as soon
+  // as the task before it is dispatched, before its event is polled.
+  TaskDesc* head = &S.desc[2];
+  int head_id = -1;
+  if (tid == 0) {
+    jit_head = ld_relaxed(&jh->head);
+    if (ai < a1) {
+      head_id = G.aot_list[ai];
+      *head = G.tasks[head_id];
+    }
+  }
   Ring ring{0, 0};
   int iter = 0;
-  uint64_t t_look = 0, t_ready = 0;
   while (true) {
     if (tid == 0) {
-      if (G.trace) t_look = globaltimer();
+      if (G.trace) S.times[0] = globaltimer();
       int cmd = -1;
       uint32_t spins = 0;
-      int head_task = (ai < a1) ? G.aot_list[ai] : -1;
-      int head_dep = (head_task >= 0) ? G.tasks[head_task].dep : G.end;
+      const int head_dep = (head_id >= 0) ? head->dep : G.end;
       while (!S.ctrl[2]) {
         uint32_t v;
         if (ring_try_pop(jh, js, G.jit_cap, jit_head, v)) {
           cmd = (int)v;
+          S.desc[iter & 1] = G.tasks[cmd];
           break;
         }
         if (event_done(P, head_dep)) {
-          cmd = head_task;   // -1 when the end event fired
-          if (head_task >= 0) ++ai;
+          cmd = head_id;   // -1 when the end event fired
+          if (head_id >= 0) {
+            S.desc[iter & 1] = *head;
+            ++ai;
+            head_id = (ai < a1) ? G.aot_list[ai] : -1;
+            if (head_id >= 0) *head = G.tasks[head_id];
+          }
           break;
         }
         ++spins;
-        if (spins > 32) __nanosleep(spins > 4096 ? 256 : 32);
+        if (spins > 64) __nanosleep(spins > 8192 ? 128 : 16);
         if ((spins & 63u) == 0u) {
           if (aborted(P)) break;
           if (globaltimer() > deadline) {
@@ -1227,29 +1746,29 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
         }
       }
       fence_acq_rel_gpu();
-      if (G.trace) t_ready = globaltimer();
+      if (G.trace) S.times[1] = globaltimer();
       S.ctrl[iter & 1] = cmd;
     }
     consumer_sync();
     const int cmd = S.ctrl[iter & 1];
+    const int slot = iter & 1;
     ++iter;
     if (cmd < 0) break;
-    const TaskDesc t = G.tasks[cmd];
-    run_task(P, S, t, ring, deadline);
+    run_task(P, S, S.desc[slot], ring, deadline);
     consumer_sync();
     // only the leader decides to stop (at its next poll), so all consumer
     // threads leave through the same broadcast
     if (tid == 0 && !S.ctrl[2] && !aborted(P)) {
       __threadfence();
-      trigger(P, t.trig, deadline);
+      trigger(P, S.desc[slot].trig, deadline);
       if (G.trace) {
         // (task | worker << 32), looked-for, ready, done
         const uint32_t k = atomicAdd(G.trace_count, 1u);
         if (k < G.trace_cap) {
           uint64_t* r = G.trace + 4ull * k;
           r[0] = (uint64_t)(uint32_t)cmd | ((uint64_t)(uint32_t)w << 32);
-          r[1] = t_look;
-          r[2] = t_ready;
+          r[1] = S.times[0];
+          r[2] = S.times[1];
           r[3] = globaltimer();
         }
       }
@@ -1284,8 +1803,8 @@ __device__ void scheduler_role(const KernelParams& P, int s,
         }
       }
     }
-    e = __shfl_sync(0xffffffffu, e, 0);
-    stop = __shfl_sync(0xffffffffu, stop, 0);
+    e = __shfl_sync(kFull, e, 0);
+    stop = __shfl_sync(kFull, stop, 0);
     if (stop) break;
     if (e < 0) continue;
     const EventDesc ed = G.events[e];
@@ -1304,13 +1823,13 @@ __device__ void scheduler_role(const KernelParams& P, int s,
 // ------------------------------------------------------------ kernels
 __device__ __forceinline__ bool setup_smem(const KernelParams& P, uint8_t* raw,
                                            Smem& S) {
-  if (smem_addr(raw) & 1023u) {   // uniform: same address for all threads
+  if (smem_addr(raw) & 127u) {   // uniform: same address for all threads
     if (threadIdx.x == 0) raise_error(P, MPK_ERR_UNSUPPORTED);
     return false;
   }
-  S = carve(raw, P.graph.n_pages, P.dims.B);
+  S = carve(raw, P.sm);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < P.graph.n_pages; ++i) {
+    for (int i = 0; i < S.n_pages; ++i) {
       mbar_init(&S.full[i], 1);
       mbar_init(&S.empty[i], kConsumerWarps);
     }
@@ -1319,6 +1838,7 @@ __device__ __forceinline__ bool setup_smem(const KernelParams& P, uint8_t* raw,
     // an earlier step that failed leaves the abort flag up until
     // mpk_reset; read it once per CTA so all threads agree
     S.ctrl[3] = aborted(P) ? 1 : 0;
+    S.ctrl[4] = 0;
     fence_proxy_async_smem();
   }
   __syncthreads();
@@ -1366,8 +1886,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------ host side
-int smem_bytes(int n_pages, int batch) { return smem_bytes_for(n_pages, batch); }
-
 cudaError_t configure_kernels(int smem) {
   cudaError_t e = cudaFuncSetAttribute(
       mpk_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -8,7 +8,6 @@
 
 namespace mpk {
 
-int smem_bytes(int n_pages, int batch);
 cudaError_t configure_kernels(int smem);
 cudaError_t launch_megakernel(const KernelParams& P, int grid, int smem,
                               cudaStream_t stream);

@@ -13,24 +13,21 @@ namespace {
 // an output region with an input region.
 enum TensorKind {
   T_H = 0,     // residual stream entering layer l (h_l), [B, hidden]
-  T_N1,        // RMSNorm(h_l)
   T_QKV,       // [B, (Hq + 2Hkv) d]
-  T_Q,         // rotated queries [B, Hq d]
-  T_KV,        // layer l's KV cache viewed as [B, Hkv]
   T_OPART,     // attention partials [B Hkv, chunks]
   T_ATTN,      // attention output [B, Hq d]
   T_O,         // o-projection output [B, hidden]
   T_HMID,      // h_l + o
-  T_N2,        // RMSNorm(hmid)
   T_ACT,       // SwiGLU (or SiLU) activation [B, ffn]
   T_DOUT,      // down-projection output [B, hidden]
-  T_NF,        // final RMSNorm output
   T_Z,         // chained mode: W2 output
   T_LOGITS,
   T_AMAX,      // per-tile (max, argmax) [B, lm_head tiles]
   T_NEXT,
   T_NKINDS
 };
+
+constexpr int kWhole = 1 << 30;   // "to the end" of a tensor axis
 
 struct Decomposer {
   const BuildConfig& cfg;
@@ -53,17 +50,31 @@ struct Decomposer {
     t.tile = op.n++;
     return t;
   }
-  void gemv(int kind, int layer, int n_rows, int src, int k_cols, int dst,
+  // A read of a whole tensor (or, with coarse events, every read).
+  void read(BTask& t, int tensor, int r0, int r1, int c0, int c1) {
+    if (cfg.coarse_events)
+      t.reads.push_back({tensor, 0, kWhole, 0, kWhole});
+    else
+      t.reads.push_back({tensor, r0, r1, c0, c1});
+  }
+  // MatMul tiles: each reads its whole input rows (the sources of its
+  // prologue); tile 0 also writes `resid` when the prologue forms one.
+  void gemv(int kind, int layer, int n_rows, bool dual,
+            std::initializer_list<int> srcs, int k_cols, int dst, int resid,
             int extra_dst) {
     const int B = cfg.batch;
     begin_op(kind, layer);
-    auto tl = row_tiles(n_rows, cfg.gemv_rows_per_task, cfg.num_workers);
+    const int rpt =
+        B >= 8 ? cfg.mma_rows_per_task : cfg.gemv_rows_per_task;
+    auto tl = row_tiles(n_rows, rpt, cfg.num_workers,
+                        tile_row_cap(B, dual));
     for (size_t i = 0; i < tl.size(); ++i) {
       BTask& t = add_task();
       t.row0 = tl[i].first;
       t.row1 = tl[i].second;
-      t.reads.push_back({src, 0, B, 0, k_cols});
+      for (int src : srcs) read(t, src, 0, B, 0, k_cols);
       t.writes.push_back({dst, 0, B, t.row0, t.row1});
+      if (i == 0 && resid >= 0) t.writes.push_back({resid, 0, B, 0, k_cols});
       if (extra_dst >= 0)
         t.writes.push_back({extra_dst, 0, B, (int)i, (int)i + 1});
     }
@@ -73,45 +84,27 @@ struct Decomposer {
     const mpk_model_shape& s = cfg.shape;
     const int B = cfg.batch, h = s.hidden, d = s.head_dim;
     const int Hq = s.n_q_heads, Hkv = s.n_kv_heads;
-    int lm_src;
+    const int L = s.n_layers;
     if (s.chain_ffn > 0) {
-      begin_op(MPK_TASK_CHAIN_NORM, 0);
-      add_task().writes.push_back({tid(T_N1, 0), 0, B, 0, h});
-      gemv(MPK_TASK_CHAIN_UP, 0, s.chain_ffn, tid(T_N1, 0), h, tid(T_ACT, 0),
+      // x = RMSNorm(embed[token]) is the prologue of every W1 tile
+      gemv(MPK_TASK_CHAIN_UP, 0, s.chain_ffn, false, {}, h, tid(T_ACT, 0), -1,
            -1);
-      gemv(MPK_TASK_CHAIN_DOWN, 0, h, tid(T_ACT, 0), s.chain_ffn,
-           tid(T_Z, 0), -1);
-      lm_src = tid(T_Z, 0);
+      gemv(MPK_TASK_CHAIN_DOWN, 0, h, false, {tid(T_ACT, 0)}, s.chain_ffn,
+           tid(T_Z, 0), -1, -1);
+      gemv(MPK_TASK_LM_HEAD, 0, s.vocab, false, {tid(T_Z, 0)}, h,
+           tid(T_LOGITS, 0), -1, tid(T_AMAX, 0));
     } else {
       const int grp = Hq / Hkv, C = cfg.attn_chunks;
-      const int L = s.n_layers;
       for (int l = 0; l < L; ++l) {
-        begin_op(MPK_TASK_NORM1, l);
-        {
-          BTask& t = add_task();
-          if (l > 0) {
-            t.reads.push_back({tid(T_HMID, l - 1), 0, B, 0, h});
-            t.reads.push_back({tid(T_DOUT, l - 1), 0, B, 0, h});
-          }
-          t.writes.push_back({tid(T_H, l), 0, B, 0, h});
-          t.writes.push_back({tid(T_N1, l), 0, B, 0, h});
-        }
-        gemv(MPK_TASK_QKV, l, (Hq + 2 * Hkv) * d, tid(T_N1, l), h,
-             tid(T_QKV, l), -1);
-        begin_op(MPK_TASK_ROPE, l);
-        for (int b = 0; b < B; ++b)
-          for (int g = 0; g < Hkv; ++g) {
-            BTask& t = add_task();
-            t.b = b;
-            t.g = g;
-            const int q0 = g * grp * d, q1 = (g + 1) * grp * d;
-            const int k0 = Hq * d + g * d, v0 = (Hq + Hkv) * d + g * d;
-            t.reads.push_back({tid(T_QKV, l), b, b + 1, q0, q1});
-            t.reads.push_back({tid(T_QKV, l), b, b + 1, k0, k0 + d});
-            t.reads.push_back({tid(T_QKV, l), b, b + 1, v0, v0 + d});
-            t.writes.push_back({tid(T_Q, l), b, b + 1, q0, q1});
-            t.writes.push_back({tid(T_KV, l), b, b + 1, g, g + 1});
-          }
+        // prologue: h_l = hmid_{l-1} + dout_{l-1} (layer 0: embedding), then
+        // RMSNorm; tile 0 stores h_l
+        if (l == 0)
+          gemv(MPK_TASK_QKV, l, (Hq + 2 * Hkv) * d, false, {}, h,
+               tid(T_QKV, l), tid(T_H, l), -1);
+        else
+          gemv(MPK_TASK_QKV, l, (Hq + 2 * Hkv) * d, false,
+               {tid(T_HMID, l - 1), tid(T_DOUT, l - 1)}, h, tid(T_QKV, l),
+               tid(T_H, l), -1);
         begin_op(MPK_TASK_ATTN, l);
         for (int b = 0; b < B; ++b)
           for (int g = 0; g < Hkv; ++g)
@@ -120,52 +113,34 @@ struct Decomposer {
               t.b = b;
               t.g = g;
               t.c = c;
-              t.reads.push_back({tid(T_Q, l), b, b + 1, g * grp * d,
-                                 (g + 1) * grp * d});
-              t.reads.push_back({tid(T_KV, l), b, b + 1, g, g + 1});
+              const int q0 = g * grp * d, q1 = (g + 1) * grp * d;
+              const int k0 = Hq * d + g * d, v0 = (Hq + Hkv) * d + g * d;
+              read(t, tid(T_QKV, l), b, b + 1, q0, q1);
+              read(t, tid(T_QKV, l), b, b + 1, k0, k0 + d);
+              read(t, tid(T_QKV, l), b, b + 1, v0, v0 + d);
               t.writes.push_back(
                   {tid(T_OPART, l), b * Hkv + g, b * Hkv + g + 1, c, c + 1});
+              // the last chunk to finish merges (b, g): every chunk may
+              // write the group's attention output
+              t.writes.push_back({tid(T_ATTN, l), b, b + 1, q0, q1});
             }
-        begin_op(MPK_TASK_MERGE, l);
-        for (int b = 0; b < B; ++b)
-          for (int g = 0; g < Hkv; ++g) {
-            BTask& t = add_task();
-            t.b = b;
-            t.g = g;
-            t.reads.push_back(
-                {tid(T_OPART, l), b * Hkv + g, b * Hkv + g + 1, 0, C});
-            t.writes.push_back({tid(T_ATTN, l), b, b + 1, g * grp * d,
-                                (g + 1) * grp * d});
-          }
-        gemv(MPK_TASK_O, l, h, tid(T_ATTN, l), Hq * d, tid(T_O, l), -1);
-        begin_op(MPK_TASK_NORM2, l);
-        {
-          BTask& t = add_task();
-          t.reads.push_back({tid(T_H, l), 0, B, 0, h});
-          t.reads.push_back({tid(T_O, l), 0, B, 0, h});
-          t.writes.push_back({tid(T_HMID, l), 0, B, 0, h});
-          t.writes.push_back({tid(T_N2, l), 0, B, 0, h});
-        }
-        gemv(MPK_TASK_GATEUP, l, s.ffn, tid(T_N2, l), h, tid(T_ACT, l), -1);
-        gemv(MPK_TASK_DOWN, l, h, tid(T_ACT, l), s.ffn, tid(T_DOUT, l), -1);
+        gemv(MPK_TASK_O, l, h, false, {tid(T_ATTN, l)}, Hq * d, tid(T_O, l),
+             -1, -1);
+        // prologue: hmid_l = h_l + o_l, RMSNorm; tile 0 stores hmid_l
+        gemv(MPK_TASK_GATEUP, l, s.ffn, true, {tid(T_H, l), tid(T_O, l)}, h,
+             tid(T_ACT, l), tid(T_HMID, l), -1);
+        gemv(MPK_TASK_DOWN, l, h, false, {tid(T_ACT, l)}, s.ffn,
+             tid(T_DOUT, l), -1, -1);
       }
-      begin_op(MPK_TASK_FINAL_NORM, L);
-      {
-        BTask& t = add_task();
-        t.reads.push_back({tid(T_HMID, L - 1), 0, B, 0, h});
-        t.reads.push_back({tid(T_DOUT, L - 1), 0, B, 0, h});
-        t.writes.push_back({tid(T_H, L), 0, B, 0, h});
-        t.writes.push_back({tid(T_NF, 0), 0, B, 0, h});
-      }
-      lm_src = tid(T_NF, 0);
+      // prologue: the final residual sum + RMSNorm; tile 0 stores h_L
+      gemv(MPK_TASK_LM_HEAD, L, s.vocab, false,
+           {tid(T_HMID, L - 1), tid(T_DOUT, L - 1)}, h, tid(T_LOGITS, 0),
+           tid(T_H, L), tid(T_AMAX, 0));
     }
-    const int Lf = s.n_layers;
-    gemv(MPK_TASK_LM_HEAD, Lf, s.vocab, lm_src, h, tid(T_LOGITS, 0),
-         tid(T_AMAX, 0));
     const int n_lm = ops.back().n;
-    begin_op(MPK_TASK_ARGMAX, Lf);
+    begin_op(MPK_TASK_ARGMAX, L);
     BTask& t = add_task();
-    t.reads.push_back({tid(T_AMAX, 0), 0, B, 0, n_lm});
+    read(t, tid(T_AMAX, 0), 0, B, 0, n_lm);
     t.writes.push_back({tid(T_NEXT, 0), 0, B, 0, 1});
   }
 };
@@ -264,8 +239,13 @@ void fuse(std::vector<Ev>& ev) {
 
 }  // namespace
 
+int tile_row_cap(int batch, bool dual) {
+  const int page_rows = batch == 1 ? 2048 : (batch < 8 ? 64 : 128);
+  return dual ? page_rows / 2 : page_rows;
+}
+
 std::vector<std::pair<int, int>> row_tiles(int n_rows, int rows_per_task,
-                                           int num_workers) {
+                                           int num_workers, int cap_rows) {
   std::vector<std::pair<int, int>> out;
   if (rows_per_task > 0) {
     for (int s = 0; s < n_rows; s += rows_per_task)
@@ -273,12 +253,19 @@ std::vector<std::pair<int, int>> row_tiles(int n_rows, int rows_per_task,
     return out;
   }
   const int64_t U = (n_rows + 7) / 8;
-  const int64_t T = std::min<int64_t>(num_workers, U);
+  const int64_t cap_u = std::max(1, cap_rows / 8);
+  const int64_t T0 = (U + cap_u - 1) / cap_u;
+  const int64_t W = std::max(1, num_workers);
+  const int64_t T = std::max<int64_t>(1, std::min(U, W * ((T0 + W - 1) / W)));
   for (int64_t i = 0; i < T; ++i) {
     const int64_t u0 = (i * U) / T, u1 = ((i + 1) * U) / T;
     out.emplace_back((int)(8 * u0), (int)std::min<int64_t>(n_rows, 8 * u1));
   }
   return out;
+}
+
+bool attn_is_aot(int batch, int max_ctx, int chunks) {
+  return batch == 1 && chunks > 0 && (max_ctx + chunks - 1) / chunks <= 128;
 }
 
 int default_attn_chunks(int batch, int n_kv_heads, int max_ctx,
@@ -300,7 +287,9 @@ mpk_status build_tgraph(const BuildConfig& cfg_in, BuiltGraph* out,
   if (cfg.batch < 1 || cfg.num_workers < 1) return fail(MPK_ERR_INVALID_ARG, "batch and workers must be >= 1");
   if (s.hidden < 8 || s.vocab < 1) return fail(MPK_ERR_INVALID_ARG, "bad hidden/vocab");
   if (s.hidden % 8) return fail(MPK_ERR_UNSUPPORTED, "hidden must be a multiple of 8");
+  if (s.hidden > 8192) return fail(MPK_ERR_UNSUPPORTED, "hidden must be <= 8192 (RMSNorm prologue)");
   const bool chain = s.chain_ffn > 0;
+  int max_ctx = 0;
   if (chain) {
     if (s.n_layers != 0) return fail(MPK_ERR_INVALID_ARG, "chained mode needs n_layers == 0");
     if (s.chain_ffn % 8) return fail(MPK_ERR_UNSUPPORTED, "chain_ffn must be a multiple of 8");
@@ -309,19 +298,28 @@ mpk_status build_tgraph(const BuildConfig& cfg_in, BuiltGraph* out,
         s.page_size < 1 || s.max_pages_per_seq < 1)
       return fail(MPK_ERR_INVALID_ARG, "bad decoder shape");
     if (s.n_q_heads % s.n_kv_heads) return fail(MPK_ERR_INVALID_ARG, "n_q_heads % n_kv_heads != 0");
-    if (s.head_dim % 8 || s.head_dim < 8 || s.head_dim > 128)
-      return fail(MPK_ERR_UNSUPPORTED, "head_dim must be a multiple of 8 in [8, 128]");
-    if (s.n_q_heads / s.n_kv_heads > 16) return fail(MPK_ERR_UNSUPPORTED, "more than 16 query heads per KV head");
+    if (s.head_dim != 32 && s.head_dim != 64 && s.head_dim != 128)
+      return fail(MPK_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 128");
+    const int grp = s.n_q_heads / s.n_kv_heads;
+    if (grp != 1 && grp != 2 && grp != 4 && grp != 8)
+      return fail(MPK_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8");
     if (s.ffn % 8) return fail(MPK_ERR_UNSUPPORTED, "ffn must be a multiple of 8");
+    max_ctx = s.max_pages_per_seq * s.page_size;
     if (cfg.attn_chunks <= 0)
-      cfg.attn_chunks = default_attn_chunks(cfg.batch, s.n_kv_heads,
-                                            s.max_pages_per_seq * s.page_size,
+      cfg.attn_chunks = default_attn_chunks(cfg.batch, s.n_kv_heads, max_ctx,
                                             cfg.num_workers);
   }
   if (cfg.batch > 16) return fail(MPK_ERR_UNSUPPORTED, "batch > 16");
-  if (cfg.gemv_rows_per_task < 0 || cfg.gemv_rows_per_task % 8)
-    return fail(MPK_ERR_INVALID_ARG, "gemv_rows_per_task must be a multiple of 8");
+  if (cfg.gemv_rows_per_task < 0 || cfg.gemv_rows_per_task % 8 ||
+      cfg.mma_rows_per_task < 0 || cfg.mma_rows_per_task % 8)
+    return fail(MPK_ERR_INVALID_ARG, "rows per task must be a multiple of 8");
+  {
+    const int rpt = cfg.batch >= 8 ? cfg.mma_rows_per_task : cfg.gemv_rows_per_task;
+    if (rpt > tile_row_cap(cfg.batch, true))
+      return fail(MPK_ERR_UNSUPPORTED, "rows per task above the tile cap");
+  }
   if (chain) cfg.attn_chunks = 0;
+  const bool attn_aot = !chain && attn_is_aot(cfg.batch, max_ctx, cfg.attn_chunks);
 
   BuiltGraph g;
   g.cfg = cfg;
@@ -457,7 +455,7 @@ mpk_status build_tgraph(const BuildConfig& cfg_in, BuiltGraph* out,
     if (kind == MPK_TASK_EMPTY) {
       g.launch[p] = MPK_LAUNCH_INLINE;
       g.worker[p] = -1;
-    } else if (kind == MPK_TASK_ATTN || kind == MPK_TASK_MERGE) {
+    } else if (kind == MPK_TASK_ATTN && !attn_aot) {
       g.launch[p] = MPK_LAUNCH_JIT;
       g.worker[p] = -1;
     } else {

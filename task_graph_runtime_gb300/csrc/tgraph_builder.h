@@ -38,8 +38,10 @@ struct BuildConfig {
   mpk_model_shape shape;
   int batch;
   int num_workers;
-  int gemv_rows_per_task;
-  int attn_chunks;       // resolved (> 0 for decoder mode)
+  int gemv_rows_per_task;  // batch < 8 (0: default)
+  int mma_rows_per_task;   // batch >= 8 (0: default)
+  int attn_chunks;         // resolved (> 0 for decoder mode)
+  int coarse_events;       // 1: operator-level events (Figure 4c ablation)
 };
 
 struct BuiltGraph {
@@ -54,10 +56,21 @@ struct BuiltGraph {
   int root_lin = 0, end_lin = 0;   // linear ids of the root and end events
 };
 
-// Row tiling of an N-row MatMul: explicit size, or min(W, ceil(N/8)) tiles
-// with multiple-of-8 sizes (boundaries at floor(i*U/T) units of 8 rows).
+// Most output rows one MatMul tile may hold: its weight pages' rows land in
+// a per-tile result buffer and, at batch > 1, in per-thread accumulators.
+// Page rows: 2048 at batch 1, 64 at batch 2..7, 128 at batch >= 8; a
+// gate/up tile holds two page rows per output row.
+int tile_row_cap(int batch, bool dual);
+
+// Row tiling of an N-row MatMul: explicit size (a multiple of 8, at most the
+// cap), or T = W * ceil(T0 / W) tiles (at most U = ceil(N/8)) with
+// T0 = ceil(U / (cap/8)), boundaries at 8 * floor(i*U/T) rows.
 std::vector<std::pair<int, int>> row_tiles(int n_rows, int rows_per_task,
-                                           int num_workers);
+                                           int num_workers, int cap_rows);
+
+// Attention chunks are AOT (their KV prefetched into the ring) at batch 1
+// when no chunk can exceed 128 tokens, JIT otherwise.
+bool attn_is_aot(int batch, int max_ctx, int chunks);
 
 int default_attn_chunks(int batch, int n_kv_heads, int max_ctx,
                         int num_workers);

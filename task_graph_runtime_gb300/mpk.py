@@ -25,9 +25,8 @@ STATUS_NAMES = {
     9: "MPK_ERR_GRAPH_INVALID", 10: "MPK_ERR_NOT_BOUND"}
 globals().update({v: k for k, v in STATUS_NAMES.items()})
 
-TASK_KINDS = ["empty", "norm1", "qkv", "rope", "attn", "merge", "o", "norm2",
-              "gateup", "down", "final_norm", "lm_head", "argmax",
-              "chain_norm", "chain_up", "chain_down"]
+TASK_KINDS = ["empty", "qkv", "attn", "o", "gateup", "down", "lm_head",
+              "argmax", "chain_up", "chain_down"]
 MODE_MEGAKERNEL, MODE_KPO, MODE_KPO_GRAPH = 0, 1, 2
 LAYER_TENSORS = ["ln1", "wqkv", "q_norm", "k_norm", "wo", "ln2", "wgu", "wd"]
 
@@ -51,10 +50,13 @@ class ModelShape(ctypes.Structure):
 class TileSizes(ctypes.Structure):
     _fields_ = [("num_workers", ctypes.c_int),
                 ("gemv_rows_per_task", ctypes.c_int),
+                ("mma_rows_per_task", ctypes.c_int),
                 ("attn_chunks", ctypes.c_int),
                 ("num_sched_sms", ctypes.c_int),
                 ("sched_warps_per_sm", ctypes.c_int),
-                ("smem_pages", ctypes.c_int)]
+                ("smem_pages", ctypes.c_int),
+                ("l2_prefetch_pages", ctypes.c_int),
+                ("coarse_events", ctypes.c_int)]
 
 
 class _Weights(ctypes.Structure):
@@ -117,6 +119,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mpk_debug_add_event_count": ([vp, i, i], st),
         "mpk_debug_set_trace": ([vp, i], st),
         "mpk_debug_read_trace": ([vp, vp, i, ctypes.POINTER(i)], st),
+        "mpk_debug_read_hidden": ([vp, i, vp], st),
         "mpk_decode_step_noalloc": ([vp, ctypes.POINTER(_Weights), vp,
                                      ctypes.POINTER(_KVCache), vp, vp, vp,
                                      vp], st),
@@ -235,12 +238,15 @@ class Graph:
                  gemv_rows_per_task: int = 0, attn_chunks: int = 0,
                  num_sched_sms: int = 0, sched_warps_per_sm: int = 0,
                  smem_pages: int = 0, page_size: int = 16,
-                 max_pages_per_seq: int = 1):
+                 max_pages_per_seq: int = 1, mma_rows_per_task: int = 0,
+                 l2_prefetch_pages: int = 0, coarse_events: int = 0):
         self.shape = shape
         self.batch = batch
         self.c_shape = model_shape(shape, page_size, max_pages_per_seq)
-        self.tiles = TileSizes(num_workers, gemv_rows_per_task, attn_chunks,
-                               num_sched_sms, sched_warps_per_sm, smem_pages)
+        self.tiles = TileSizes(num_workers, gemv_rows_per_task,
+                               mma_rows_per_task, attn_chunks, num_sched_sms,
+                               sched_warps_per_sm, smem_pages,
+                               l2_prefetch_pages, coarse_events)
         self.handle = mpk_build_tgraph(self.c_shape, self.tiles, batch)
         self._keep = None
 
@@ -300,6 +306,15 @@ class Graph:
             self.handle, buf.ctypes.data, capacity, ctypes.byref(n)),
             "mpk_debug_read_trace")
         return buf[:n.value]
+
+    def read_hidden(self, layer: int) -> np.ndarray:
+        """bf16 bits [batch, hidden] of the residual stream entering decoder
+        layer ``layer`` (``n_layers``: the final RMSNorm's input) in the last
+        step."""
+        out = np.zeros((self.batch, self.shape.hidden), np.uint16)
+        _check(load_library().mpk_debug_read_hidden(
+            self.handle, layer, out.ctypes.data), "mpk_debug_read_hidden")
+        return out
 
     def close(self):
         if self.handle:

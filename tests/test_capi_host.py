@@ -63,8 +63,11 @@ CASES = [
     ("tiny_w7", "tiny", 1, dict(num_workers=7)),
     ("tiny_w148", "tiny", 1, dict(num_workers=148)),
     ("tiny_b3_c3", "tiny", 3, dict(num_workers=5, attn_chunks=3)),
-    ("tiny_r40", "tiny", 2, dict(num_workers=6, gemv_rows_per_task=40,
+    ("tiny_r24", "tiny", 2, dict(num_workers=6, gemv_rows_per_task=24,
                                   attn_chunks=2)),
+    ("tiny_c1", "tiny", 1, dict(num_workers=4, attn_chunks=1)),
+    ("tiny_coarse", "tiny", 1, dict(num_workers=4, coarse_events=1)),
+    ("tiny_b8_mma16", "tiny", 8, dict(num_workers=5, mma_rows_per_task=16)),
     ("llama1b", "llama1b", 1, dict(num_workers=148)),
     ("qwen3_8b", "qwen3_8b", 1, dict(num_workers=148)),
     ("qwen3_8b_b16", "qwen3_8b_b16", 16, dict(num_workers=148)),
@@ -86,7 +89,9 @@ def test_cpp_builder_matches_oracle_builder(mpk_lib, case):
     ref = tgraph.build(shape, B, mp * page,
                        tgraph.Tiles(kw["num_workers"],
                                     kw.get("gemv_rows_per_task", 0),
-                                    kw.get("attn_chunks", 0)))
+                                    kw.get("attn_chunks", 0),
+                                    kw.get("mma_rows_per_task", 0),
+                                    kw.get("coarse_events", 0)))
     assert ex["n_tasks"] == len(ref.order)
     assert ex["n_events"] == len(ref.ev_count)
     assert ex["n_empty"] == ref.n_empty

@@ -182,7 +182,8 @@ def test_unsatisfiable_event_times_out_and_recovers(tiny):
     g.bind(Wd)
     ex = g.export()
     # the event the QKV tiles of layer 0 wait on
-    first_qkv = int(np.flatnonzero(ex["task_kind"] == 2)[0])
+    first_qkv = int(np.flatnonzero(
+        ex["task_kind"] == mpk.TASK_KINDS.index("qkv"))[0])
     e = int(ex["task_dep"][first_qkv])
     g.add_event_count(e, +1)
     g.set_wait_timeout_ms(300)

@@ -120,8 +120,14 @@ SMALL_CASES = [
     ("tiny_w7", synth.WORKLOADS["tiny"].shape, 1, 144, tgraph.Tiles(7)),
     ("tiny_b3", synth.WORKLOADS["tiny"].shape, 3, 144,
      tgraph.Tiles(5, attn_chunks=3)),
-    ("tiny_r40", synth.WORKLOADS["tiny"].shape, 2, 144,
-     tgraph.Tiles(6, gemv_rows_per_task=40, attn_chunks=2)),
+    ("tiny_r24", synth.WORKLOADS["tiny"].shape, 2, 144,
+     tgraph.Tiles(6, gemv_rows_per_task=24, attn_chunks=2)),
+    ("tiny_c1_jit", synth.WORKLOADS["tiny"].shape, 1, 144,
+     tgraph.Tiles(4, attn_chunks=1)),
+    ("tiny_coarse", synth.WORKLOADS["tiny"].shape, 1, 144,
+     tgraph.Tiles(4, coarse_events=1)),
+    ("tiny_b8_mma", synth.WORKLOADS["tiny"].shape, 8, 144,
+     tgraph.Tiles(5, mma_rows_per_task=16)),
     ("chain", synth.ModelShape(0, 64, 1, 1, 32, 0, 96, chain_ffn=160), 2, 0,
      tgraph.Tiles(3)),
 ]
@@ -178,31 +184,81 @@ def test_normalised_and_contiguous(built):
 
 
 def test_launch_classes_and_aot_round_robin(built):
+    """Empty tasks inline; attention chunks JIT unless they are equal and
+    small (batch 1, <= 128 tokens); every other task AOT, dealt round-robin
+    in linear order (MPK summary, "Design space": hybrid JIT/AOT)."""
     k = 0
     W = max(w for w in built.worker) + 1
+    kinds = {built.tasks[t].kind for t in built.order}
+    attn_jit = None
     for pos, t in enumerate(built.order):
         kind = built.tasks[t].kind
         if kind == "empty":
             assert built.launch[pos] == tgraph.INLINE
-        elif kind in ("attn", "merge"):
-            assert built.launch[pos] == tgraph.JIT
-        else:
-            assert built.launch[pos] == tgraph.AOT
-            assert built.worker[pos] == k % W
-            k += 1
+            continue
+        if kind == "attn":
+            jit = built.launch[pos] == tgraph.JIT
+            assert attn_jit in (None, jit)     # one class for the operator
+            attn_jit = jit
+            if jit:
+                assert built.worker[pos] == -1
+                continue
+        assert built.launch[pos] == tgraph.AOT
+        assert built.worker[pos] == k % W
+        k += 1
+    if "attn" in kinds:
+        n_attn = sum(1 for t in built.tasks if t.kind == "attn")
+        B = 1 + max(t.b for t in built.tasks if t.kind == "attn")
+        assert attn_jit == (B > 1 or built.n_chunks == 1)
 
 
 def test_row_tiles_cover_rows():
-    for n in (8, 64, 688, 1000, 6144, 151936):
+    """Default tiles: contiguous, multiples of 8 rows, within the cap, a
+    multiple of W of them unless every tile is one 8-row unit, sizes within
+    one unit of each other."""
+    for n in (8, 64, 688, 1000, 6144, 12288, 151936):
         for W in (1, 7, 148):
-            tl = tgraph.row_tiles(n, tgraph.Tiles(W))
-            assert tl[0][0] == 0 and tl[-1][1] == n
-            assert all(a[1] == b[0] for a, b in zip(tl, tl[1:]))
-            assert all(r0 % 8 == 0 and r1 > r0 for r0, r1 in tl)
-            assert len(tl) <= W
-            sizes = [r1 - r0 for r0, r1 in tl[:-1]]
-            if sizes:
-                assert max(sizes) - min(sizes) <= 8
+            for cap in (32, 64, 128, 1024, 2048):
+                tl = tgraph.row_tiles(n, 0, W, cap)
+                assert tl[0][0] == 0 and tl[-1][1] == n
+                assert all(a[1] == b[0] for a, b in zip(tl, tl[1:]))
+                assert all(r0 % 8 == 0 and r1 > r0 for r0, r1 in tl)
+                assert all(r1 - r0 <= cap for r0, r1 in tl)
+                U = -(-n // 8)
+                assert len(tl) % W == 0 or len(tl) == U
+                sizes = [r1 - r0 for r0, r1 in tl[:-1]]
+                if sizes:
+                    assert max(sizes) - min(sizes) <= 8
+
+
+def test_tile_caps_by_batch():
+    assert tgraph.tile_row_cap(1, False) == 2048
+    assert tgraph.tile_row_cap(1, True) == 1024
+    assert tgraph.tile_row_cap(4, False) == 64
+    assert tgraph.tile_row_cap(16, True) == 64
+
+
+def test_coarse_events_are_operator_level():
+    """Figure 4c: with operator-level events every task of an operator
+    waits for every task of each operator it reads, so one event separates
+    consecutive operators."""
+    shape = synth.WORKLOADS["tiny"].shape
+    fine = tgraph.build(shape, 1, 144, tgraph.Tiles(4))
+    coarse = tgraph.build(shape, 1, 144, tgraph.Tiles(4, coarse_events=1))
+    assert (len(coarse.order) - coarse.n_empty ==
+            len(fine.order) - fine.n_empty)
+    # every attention chunk of layer 0 waits on the event the whole qkv
+    # operator triggers (fine: only on the tiles holding its head's columns)
+    attn = [p for p, t in enumerate(coarse.order)
+            if coarse.tasks[t].kind == "attn" and coarse.tasks[t].layer == 0]
+    deps = {coarse.dep[p] for p in attn}
+    assert len(deps) == 1
+    qkv0 = [t for t in coarse.tasks if t.kind == "qkv" and t.layer == 0]
+    e = deps.pop()
+    assert coarse.ev_count[e] >= len(qkv0)
+    fine_attn = [p for p, t in enumerate(fine.order)
+                 if fine.tasks[t].kind == "attn" and fine.tasks[t].layer == 0]
+    assert len({fine.dep[p] for p in fine_attn}) > 1
 
 
 def test_random_chains_properties():
