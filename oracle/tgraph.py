@@ -99,25 +99,40 @@ class Op:
     n_tasks: int
 
 
-def tile_row_cap(batch: int, dual: bool) -> int:
-    """Most output rows of one MatMul tile: 2048 weight rows at batch 1, 64
-    at batch 2..7, 128 at batch >= 8; a gate/up tile streams two weight rows
-    per output row."""
-    rows = 2048 if batch == 1 else (64 if batch < 8 else 128)
-    return rows // 2 if dual else rows
+def tile_row_cap(batch: int, dual: bool, K: int) -> int:
+    """Most output rows of one MatMul tile with reduction length K.  Batch 1:
+    a row's dot product is split into K // 2048 partial sums when K is a
+    multiple of 2048, else into 1 (when 32 KB pages hold 8 or more rows of
+    max(1, 16384 // K)) or 8 // rows partials; the tile's partials fit 2560
+    floats.  Batch 2..7: 64 weight rows; batch >= 8: 128.  A gate/up tile
+    streams two weight rows per output row.  Rounded down to a multiple of
+    8."""
+    if batch == 1:
+        if K % 2048 == 0:
+            parts = K // 2048
+        else:
+            rpp = max(1, 16384 // K)
+            parts = 1 if rpp >= 8 else 8 // rpp
+        rows = 2560 // parts
+    else:
+        rows = 64 if batch < 8 else 128
+    if dual:
+        rows //= 2
+    return max(8, rows // 8 * 8)
 
 
 def row_tiles(n_rows: int, rows_per_task: int, num_workers: int,
-              cap: int) -> List[Tuple[int, int]]:
+              cap: int, unit: int = 8) -> List[Tuple[int, int]]:
     """Split n_rows output rows into tiles.  Explicit size R: tiles of R
-    rows, the last one ragged.  Default: U = ceil(N/8) units of 8 rows,
-    T0 = ceil(U / (cap/8)) tiles at least, rounded up to a multiple of the
-    worker count W and clipped to U; unit boundaries at floor(i * U / T)."""
+    rows, the last one ragged.  Default: U = ceil(N/unit) units of `unit`
+    rows (1 at batch 1, 8 otherwise), T0 = ceil(U / (cap/unit)) tiles at
+    least, rounded up to a multiple of the worker count W and clipped to U;
+    unit boundaries at floor(i * U / T)."""
     if rows_per_task > 0:
         R = rows_per_task
         return [(s, min(n_rows, s + R)) for s in range(0, n_rows, R)]
-    U = -(-n_rows // 8)
-    cap_u = max(1, cap // 8)
+    U = -(-n_rows // unit)
+    cap_u = max(1, cap // unit)
     T0 = -(-U // cap_u)
     W = max(1, num_workers)
     T = max(1, min(U, W * (-(-T0 // W))))
@@ -125,7 +140,7 @@ def row_tiles(n_rows: int, rows_per_task: int, num_workers: int,
     for i in range(T):
         u0 = (i * U) // T
         u1 = ((i + 1) * U) // T
-        out.append((8 * u0, min(n_rows, 8 * u1)))
+        out.append((unit * u0, min(n_rows, unit * u1)))
     return out
 
 
@@ -173,7 +188,11 @@ def decompose(shape, batch: int, max_ctx: int, tiles: Tiles):
              extra_write=None):
         rpt = tiles.mma_rows_per_task if B >= 8 else tiles.gemv_rows_per_task
         specs = []
-        tl = row_tiles(n_rows, rpt, tiles.num_workers, tile_row_cap(B, dual))
+        cap = tile_row_cap(B, dual, k_cols)
+        if rpt > cap:
+            raise ValueError("rows per task above the tile cap")
+        tl = row_tiles(n_rows, rpt, tiles.num_workers, cap,
+                       1 if B == 1 else 8)
         for i, (r0, r1) in enumerate(tl):
             w = [(dst, 0, B, r0, r1)]
             if i == 0 and resid is not None:

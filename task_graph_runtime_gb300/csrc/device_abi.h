@@ -52,25 +52,52 @@ struct RingHdr {
   uint32_t pad1[31];
 };
 
-// Weight pages: 8 matrix rows x up to 2048 columns, each row one
-// contiguous bulk copy, rows kPagePitch bytes apart (16 bytes of skew per
-// row keep ldmatrix reads of 8 rows free of bank conflicts).
+// Weight pages.
+// Batch 1: the rows [i, i + n) of a tile are n * K contiguous elements, so
+// pages are single contiguous bulk copies of at most 32 KB.  When K is a
+// multiple of 2048 ("flat" pages) a page is the next 16384 elements of the
+// tile's row stream and each consumer warp dots one 2048-element slice of
+// one row (K / 2048 partials per row); otherwise a page holds
+// b1_rows_per_page(K) whole rows, each split over b1_warps_per_row(K)
+// warps.
+// Batch > 1: 8 matrix rows x up to 2048 columns, each row one bulk copy,
+// rows kPagePitch bytes apart (16 bytes of skew per row keep ldmatrix reads
+// of 8 rows free of bank conflicts).
+constexpr int kContigPageBytes = 32768;
 constexpr int kPageRows = 8;
 constexpr int kSegCols = 2048;
 constexpr int kPagePitch = kSegCols * 2 + 16;          // 4112
 constexpr int kPageBytes = kPageRows * kPagePitch;     // 32896
 constexpr int kAttnMaxTokens = 128;                    // per prefetched chunk
+constexpr int kB1Partials = 2560;   // batch-1 row partial sums per tile
+
+#if defined(__CUDACC__)
+#define MPK_HD __host__ __device__
+#else
+#define MPK_HD
+#endif
+MPK_HD inline bool b1_flat(int K) { return K % kSegCols == 0; }
+MPK_HD inline int b1_rows_per_page(int K) {
+  const int r = (kContigPageBytes / 2) / K;
+  return r < 1 ? 1 : r;
+}
+MPK_HD inline int b1_warps_per_row(int K) {
+  if (b1_flat(K)) return K / kSegCols;
+  const int r = b1_rows_per_page(K);
+  return r >= 8 ? 1 : 8 / r;
+}
 
 // Byte offsets of the regions of a worker CTA's dynamic shared memory.
 struct SmemLayout {
-  int n_pages;      // ring slots of kPageBytes
+  int n_pages;      // ring slots
+  int page_bytes;   // slot size: kContigPageBytes (batch 1) or kPageBytes
   int xs;           // activation staging / attention scratch
   int xs_bytes;
   int res;          // MatMul row results (fp32)
   int res_floats;
   int bars;         // full[n_pages], empty[n_pages] mbarriers
   int ctrl;         // control words + staged task descriptors
-  int scratch;      // small reductions (1 KB)
+  int scratch;      // small reductions (512 bytes)
   int total;
 };
 

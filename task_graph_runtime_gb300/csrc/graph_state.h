@@ -14,7 +14,7 @@ namespace mpk_detail {
 
 constexpr uint32_t kJitCap = 1024;
 constexpr uint32_t kSchedCap = 4096;
-constexpr int kDefaultPfPages = 8;
+constexpr int kDefaultPfPages = 0;
 constexpr int kSmemLimit = 232448;   // 227 KB per block on sm_100-class
 
 template <typename T>

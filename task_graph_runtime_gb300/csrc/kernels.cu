@@ -13,14 +13,16 @@
 //     (and the KV cache of earlier tokens) never depend on an event;
 //   "关键实现细节" 2 -- task descriptors prefetched before dequeue.
 //
-// GB300 layout of a worker CTA (one per SM, 288 threads):
-//   warp 8      -- producer: walks this worker's AOT task list.  Weight
-//                  pages (8 matrix rows x <= 2048 columns) arrive by one
-//                  contiguous 1-D bulk copy (cp.async.bulk) per row; AOT
-//                  attention tasks get their KV chunk the same way.  A
-//                  second cursor runs `pf_pages` pages further ahead and
-//                  prefetches them into L2 (cp.async.bulk.prefetch.L2), so
-//                  HBM keeps streaming while the ring is full at an event;
+// GB300 layout of a worker CTA (one per SM, 320 threads):
+//   warps 8, 9  -- producers: both walk this worker's AOT task list and
+//                  take alternate pages of it (two independent bulk-copy
+//                  streams per SM sustain more HBM bandwidth than one).
+//                  Weight pages arrive by 1-D bulk copies (cp.async.bulk):
+//                  one contiguous copy of up to 32 KB at batch 1, one per
+//                  matrix row at batch > 1; AOT attention tasks get their
+//                  KV chunk the same way.  Optionally a look-ahead cursor
+//                  prefetches pages into L2 (cp.async.bulk.prefetch.L2)
+//                  while the consumers wait on an event;
 //   warps 0..7  -- consumers: poll events and the JIT queue, run task bodies,
 //                  release pages, trigger events.
 // MatMul tiles run on CUDA cores at batch < 8 and on tensor cores
@@ -39,7 +41,8 @@ namespace mpk {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kProducerWarps = 2;   // two bulk-copy streams per SM
+constexpr int kThreads = kConsumers + 32 * kProducerWarps;
 constexpr int kMaxRingPages = 8;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -69,6 +72,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
@@ -240,6 +254,7 @@ struct Smem {
   uint64_t* times;    // [2] trace: looked-for, ready
   float* scratch;
   int n_pages;
+  int page_bytes;
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* base, const SmemLayout& L) {
@@ -254,6 +269,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const SmemLayout& L) {
   s.times = reinterpret_cast<uint64_t*>(base + L.ctrl + 160);
   s.scratch = reinterpret_cast<float*>(base + L.scratch);
   s.n_pages = L.n_pages;
+  s.page_bytes = L.page_bytes;
   return s;
 }
 
@@ -269,7 +285,7 @@ struct Ring {
   }
 };
 __device__ __forceinline__ uint8_t* page_ptr(const Smem& S, uint32_t slot) {
-  return S.ring + (size_t)slot * kPageBytes;
+  return S.ring + (size_t)slot * S.page_bytes;
 }
 
 // Bounded wait for a ring page, by every consumer thread (each observes the
@@ -326,17 +342,22 @@ __device__ __forceinline__ bool is_gemv(int kind) {
          kind == MPK_TASK_CHAIN_DOWN;
 }
 
-// Geometry of one MatMul task.  Its weight rows are streamed as pages of 8
-// matrix rows (dual gate/up tiles: 4 gate rows then the matching 4 up rows)
-// by at most 2048 columns.  Page order: row groups outer at batch 1 (the
-// whole activation row is staged once), column segments outer at batch > 1
-// (one segment of every sequence's activation is staged at a time).
+// Geometry of one MatMul task.
+// Batch 1: the tile's rows are streamed as contiguous pages (a gate/up
+// tile: its gate rows, then its up rows), `pph` pages per half: flat pages
+// of 16384 elements, or pages of `rpp` whole rows; row partial sums land in
+// S.res[(half * rows + o) * wpr + part].
+// Batch > 1: pages of 8 matrix rows (gate/up tiles: 4 gate rows then the
+// matching 4 up rows) by at most 2048 columns, column segments outer (one
+// segment of every sequence's activation is staged at a time); results land
+// in S.res[b * RP + page row].
 struct Gemv {
   int kind, layer;
   int row0, rows;       // output rows [row0, row0 + rows)
   int K, N;             // reduction length, output width
   int dual, up_off;
-  int ngroups, nsegs, seg_outer;
+  int b1, flat, rpp, wpr, pph;
+  int ngroups, nsegs;
   const uint16_t* W;
 };
 
@@ -392,19 +413,40 @@ __device__ Gemv gemv_geom(const KernelParams& P, const TaskDesc& t) {
   const int gsize = g.dual ? 4 : kPageRows;
   g.ngroups = (g.rows + gsize - 1) / gsize;
   g.nsegs = (g.K + kSegCols - 1) / kSegCols;
-  g.seg_outer = D.B > 1 ? 1 : 0;
+  g.b1 = D.B == 1 ? 1 : 0;
+  g.flat = b1_flat(g.K) ? 1 : 0;
+  g.rpp = b1_rows_per_page(g.K);
+  g.wpr = b1_warps_per_row(g.K);
+  constexpr int kFlatElems = kContigPageBytes / 2;
+  g.pph = g.flat ? (int)(((int64_t)g.rows * g.K + kFlatElems - 1) / kFlatElems)
+                 : (g.rows + g.rpp - 1) / g.rpp;
   return g;
 }
 
+__device__ __forceinline__ int gemv_pages(const Gemv& g) {
+  return g.b1 ? (g.dual ? 2 : 1) * g.pph : g.ngroups * g.nsegs;
+}
+
+// Batch 1: page p of half `half` starts `e0` elements into that half's
+// row stream and holds `ne` elements; returns the address of its first one.
+__device__ __forceinline__ const uint16_t* b1_page(const Gemv& g, int p,
+                                                   int& half, int64_t& e0,
+                                                   int& ne) {
+  half = p / g.pph;
+  const int q = p - half * g.pph;
+  const int64_t total = (int64_t)g.rows * g.K;
+  e0 = g.flat ? (int64_t)q * (kContigPageBytes / 2)
+              : (int64_t)q * g.rpp * g.K;
+  const int64_t span = g.flat ? (kContigPageBytes / 2) : (int64_t)g.rpp * g.K;
+  ne = (int)min(span, total - e0);
+  return g.W + ((int64_t)(half ? g.up_off : 0) + g.row0) * g.K + e0;
+}
+
+// Batch > 1: page p is row group j of column segment s.
 __device__ __forceinline__ void page_coords(const Gemv& g, int p, int& j,
                                             int& s) {
-  if (g.seg_outer) {
-    s = p / g.ngroups;
-    j = p - s * g.ngroups;
-  } else {
-    j = p / g.nsegs;
-    s = p - j * g.nsegs;
-  }
+  s = p / g.ngroups;
+  j = p - s * g.ngroups;
 }
 // Weight-matrix row held in row i (0..7) of group j's pages.
 __device__ __forceinline__ int page_wrow(const Gemv& g, int j, int i,
@@ -425,6 +467,18 @@ __device__ __forceinline__ int page_wrow(const Gemv& g, int j, int i,
 __device__ void issue_gemv_page(const Gemv& g, int p, uint8_t* page,
                                 uint64_t* bar, uint64_t policy) {
   const int lane = threadIdx.x & 31;
+  if (g.b1) {
+    // one contiguous copy of n whole rows
+    if (lane == 0) {
+      int half, ne;
+      int64_t e0;
+      const uint16_t* src = b1_page(g, p, half, e0, ne);
+      const uint32_t bytes = (uint32_t)ne * 2u;
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_g2s(page, src, bytes, bar, policy);
+    }
+    return;
+  }
   int j, s;
   page_coords(g, p, j, s);
   const int c0 = s * kSegCols;
@@ -441,6 +495,15 @@ __device__ void issue_gemv_page(const Gemv& g, int p, uint8_t* page,
 }
 __device__ void prefetch_gemv_page(const Gemv& g, int p) {
   const int lane = threadIdx.x & 31;
+  if (g.b1) {
+    if (lane == 0) {
+      int half, ne;
+      int64_t e0;
+      const uint16_t* src = b1_page(g, p, half, e0, ne);
+      prefetch_l2(src, (uint32_t)ne * 2u);
+    }
+    return;
+  }
   if (lane >= kPageRows) return;
   int j, s;
   page_coords(g, p, j, s);
@@ -460,17 +523,17 @@ __device__ __forceinline__ void chunk_range(int c, int n, int C, int& t0,
 }
 
 // KV chunk of an AOT attention task: the cached tokens [t0, min(t1, pos))
-// into the K page and the V page (token-major rows of d values), one bulk
-// copy per run of tokens inside one KV page.  Lane 0 only.
-__device__ void issue_attn_pages(const KernelParams& P, const TaskDesc& t,
-                                 uint8_t* kpage, uint64_t* kbar,
-                                 uint8_t* vpage, uint64_t* vbar,
-                                 uint64_t policy) {
+// into the K page (which == 0) or the V page (which == 1) as token-major
+// rows of d values, one bulk copy per run of tokens inside one KV page.
+// Lane 0 only.
+__device__ void issue_attn_page(const KernelParams& P, const TaskDesc& t,
+                                int which, uint8_t* page, uint64_t* bar,
+                                uint64_t policy) {
   const Dims& D = P.dims;
   const int b = t.b, pos = __ldcg(P.step.seq_lens + b);
   const int n = pos + 1;
   int t0 = 0, t1 = 0;
-  bool ok = pos >= 0 && n <= D.max_ctx;
+  const bool ok = pos >= 0 && n <= D.max_ctx;
   if (ok) chunk_range(t.c, n, D.C, t0, t1);
   const int te = ok ? min(min(t1, pos), t0 + kAttnMaxTokens) : 0;
   const int P_ = D.page_size, d = D.d;
@@ -479,29 +542,26 @@ __device__ void issue_attn_pages(const KernelParams& P, const TaskDesc& t,
   const int64_t head_elems = (int64_t)P_ * d;
   const int64_t layer_elems =
       (int64_t)t.layer * P.step.num_pages * D.Hkv * head_elems;
+  const uint16_t* pool = which ? P.step.v_pool : P.step.k_pool;
   uint32_t total = 0;
   for (int tok = t0; tok < te;) {
     const int run_end = min(te, (tok / P_ + 1) * P_);
-    const int page = __ldg(pt + tok / P_);
-    if (page >= 0 && page < P.step.num_pages)
+    const int pg = __ldg(pt + tok / P_);
+    if (pg >= 0 && pg < P.step.num_pages)
       total += (uint32_t)(run_end - tok) * row_bytes;
     else
       raise_error(P, MPK_ERR_KV_PAGE);
     tok = run_end;
   }
-  mbar_arrive_expect_tx(kbar, total);
-  mbar_arrive_expect_tx(vbar, total);
+  mbar_arrive_expect_tx(bar, total);
   for (int tok = t0; tok < te;) {
     const int run_end = min(te, (tok / P_ + 1) * P_);
-    const int page = __ldg(pt + tok / P_);
-    if (page >= 0 && page < P.step.num_pages) {
-      const int64_t off = layer_elems +
-                          ((int64_t)page * D.Hkv + t.g) * head_elems +
+    const int pg = __ldg(pt + tok / P_);
+    if (pg >= 0 && pg < P.step.num_pages) {
+      const int64_t off = layer_elems + ((int64_t)pg * D.Hkv + t.g) * head_elems +
                           (int64_t)(tok % P_) * d;
-      const uint32_t bytes = (uint32_t)(run_end - tok) * row_bytes;
-      const size_t dst = (size_t)(tok - t0) * row_bytes;
-      bulk_g2s(kpage + dst, P.step.k_pool + off, bytes, kbar, policy);
-      bulk_g2s(vpage + dst, P.step.v_pool + off, bytes, vbar, policy);
+      bulk_g2s(page + (size_t)(tok - t0) * row_bytes, pool + off,
+               (uint32_t)(run_end - tok) * row_bytes, bar, policy);
     }
     tok = run_end;
   }
@@ -527,7 +587,7 @@ __device__ __forceinline__ int ring_pages_of(const KernelParams& P,
                                              const TaskDesc& t, Gemv* g) {
   if (is_gemv(t.kind)) {
     *g = gemv_geom(P, t);
-    return g->ngroups * g->nsegs;
+    return gemv_pages(*g);
   }
   if (t.kind == MPK_TASK_ATTN && t.launch == MPK_LAUNCH_AOT) return 2;
   return 0;
@@ -566,80 +626,125 @@ struct Lookahead {
   bool gemv;
 };
 
-__device__ void lookahead(const KernelParams& P, const int32_t* list, int n,
-                          Lookahead& la, int64_t limit) {
-  while (la.count < limit && la.i < n) {
+// Advance the cursor by one page, prefetching it into L2 if asked (and if
+// it is a weight page).  False at the end of the list.
+__device__ bool la_step(const KernelParams& P, const int32_t* list, int n,
+                        Lookahead& la, bool prefetch) {
+  while (la.i < n) {
     if (la.np < 0) {
       const TaskDesc t = P.graph.tasks[list[la.i]];
       la.np = ring_pages_of(P, t, &la.g);
       la.gemv = is_gemv(t.kind);
       la.p = 0;
     }
-    if (la.p >= la.np) {
-      ++la.i;
-      la.np = -1;
-      continue;
+    if (la.p < la.np) {
+      if (prefetch && la.gemv) prefetch_gemv_page(la.g, la.p);
+      ++la.p;
+      ++la.count;
+      return true;
     }
-    if (la.gemv) prefetch_gemv_page(la.g, la.p);
-    ++la.p;
-    ++la.count;
+    ++la.i;
+    la.np = -1;
+  }
+  return false;
+}
+
+// While the consumers hold every ring page and everything issued has
+// landed -- they are waiting for an event, not for data -- prefetch the
+// next pages into L2, up to `pf` pages beyond the ring, so HBM keeps
+// streaming during the wait.  In steady streaming the newest page is still
+// in flight and nothing is prefetched.
+__device__ void prefetch_while_idle(const KernelParams& P, const Smem& S,
+                                    const int32_t* list, int n, Lookahead& la,
+                                    const Ring& ring, int last_slot,
+                                    uint32_t last_phase, int64_t copied,
+                                    int pf) {
+  const int lane = threadIdx.x & 31;
+  while (la.count < copied)
+    if (!la_step(P, list, n, la, false)) return;
+  while (la.count < copied + pf) {
+    int idle = 0;
+    if (lane == 0)
+      idle = !mbar_test(&S.empty[ring.slot], ring.phase ^ 1u) &&
+             (last_slot < 0 || mbar_test(&S.full[last_slot], last_phase)) &&
+             !aborted(P);
+    if (!__shfl_sync(kFull, idle, 0)) return;
+    if (!la_step(P, list, n, la, true)) return;
   }
 }
 
+// Producer warp `pid` of kProducerWarps: walks the task list and issues
+// the pages whose global index gp (over the whole list) has
+// gp % kProducerWarps == pid.  The ring position advances by one for every
+// page, issued here or by the other producer, so page gp lands in slot
+// gp % n_pages with phase (gp / n_pages) & 1 -- the order in which the
+// consumers take them.
 __device__ void producer_role(const KernelParams& P, const Smem& S,
-                              const int32_t* list, int n, uint64_t deadline) {
+                              const int32_t* list, int n, uint64_t deadline,
+                              int pid) {
+  static_assert(kProducerWarps == 2, "page ownership alternates");
   const int lane = threadIdx.x & 31;
   uint32_t issued[kMaxRingPages];
 #pragma unroll
   for (int i = 0; i < kMaxRingPages; ++i) issued[i] = 0;
-  Ring ring{0, 0};
   const uint64_t policy = evict_first_policy();
-  const int pf = P.dims.pf_pages;
+  const int pf = pid == 0 ? P.dims.pf_pages : 0;
   Lookahead la{0, 0, -1, 0, Gemv{}, false};
-  int64_t copied = 0;
+  Ring ring{0, 0};
+  int64_t gp = 0;
+  int last_slot = -1;
+  uint32_t last_phase = 0;
+  int turn = 0;            // gp % 2
   for (int i = 0; i < n; ++i) {
     const TaskDesc t = P.graph.tasks[list[i]];
     Gemv g;
     const int np = ring_pages_of(P, t, &g);
-    if (np == 0) continue;
-    if (is_gemv(t.kind)) {
-      for (int p = 0; p < np; ++p) {
-        if (pf > 0) lookahead(P, list, n, la, copied + 1 + pf);
-        if (!wait_empty(P, S, ring, deadline)) {
-          drain_copies(P, S, issued);
-          return;
+    // batch-1 weight pages: source pointer and length advance linearly
+    const bool lin = np > 0 && is_gemv(t.kind) && g.b1;
+    const int64_t span = lin ? (g.flat ? (int64_t)(kContigPageBytes / 2)
+                                       : (int64_t)g.rpp * g.K)
+                             : 0;
+    const int64_t total = (int64_t)g.rows * g.K;
+    int64_t e0 = 0;
+    int half = 0;
+    for (int p = 0; p < np; ++p, ++gp, turn ^= 1, ring.advance(S.n_pages)) {
+      const bool mine = turn == pid;
+      const int64_t my_e0 = e0;
+      const int my_half = half;
+      if (lin) {   // advance to the next page of the half (or the next half)
+        e0 += span;
+        if (e0 >= total) {
+          e0 = 0;
+          ++half;
         }
-        issue_gemv_page(g, p, page_ptr(S, ring.slot), &S.full[ring.slot],
-                        policy);
-        issued[ring.slot] = 1u | (ring.phase << 1);
-        ring.advance(S.n_pages);
-        ++copied;
       }
-    } else {
-      // attention: K page then V page
-      if (pf > 0) lookahead(P, list, n, la, copied + 2 + pf);
+      if (!mine) continue;
+      if (pf > 0)
+        prefetch_while_idle(P, S, list, n, la, ring, last_slot, last_phase,
+                            gp, pf);
       if (!wait_empty(P, S, ring, deadline)) {
         drain_copies(P, S, issued);
         return;
       }
-      const uint32_t ks = ring.slot;
-      issued[ring.slot] = 1u | (ring.phase << 1);
-      ring.advance(S.n_pages);
-      if (!wait_empty(P, S, ring, deadline)) {
-        // the K slot was claimed but nothing was copied into it: complete
-        // its phase so the drain below does not wait on it
-        if (lane == 0) mbar_arrive_expect_tx(&S.full[ks], 0);
-        drain_copies(P, S, issued);
-        return;
+      uint8_t* page = page_ptr(S, ring.slot);
+      uint64_t* bar = &S.full[ring.slot];
+      if (lin) {
+        if (lane == 0) {
+          const uint32_t bytes = (uint32_t)min(span, total - my_e0) * 2u;
+          const uint16_t* src =
+              g.W + ((int64_t)(my_half ? g.up_off : 0) + g.row0) * g.K + my_e0;
+          mbar_arrive_expect_tx(bar, bytes);
+          bulk_g2s(page, src, bytes, bar, policy);
+        }
+      } else if (is_gemv(t.kind)) {
+        issue_gemv_page(g, p, page, bar, policy);
+      } else if (lane == 0) {
+        issue_attn_page(P, t, p, page, bar, policy);   // p 0: K, 1: V
       }
-      const uint32_t vs = ring.slot;
-      issued[ring.slot] = 1u | (ring.phase << 1);
-      ring.advance(S.n_pages);
-      if (lane == 0)
-        issue_attn_pages(P, t, page_ptr(S, ks), &S.full[ks], page_ptr(S, vs),
-                         &S.full[vs], policy);
       __syncwarp();
-      copied += 2;
+      issued[ring.slot] = 1u | (ring.phase << 1);
+      last_slot = (int)ring.slot;
+      last_phase = ring.phase;
     }
   }
   // the consumers wait for every page before leaving, so all copies have
@@ -761,16 +866,35 @@ __device__ __forceinline__ float rms_factor(float ss, int K, float eps) {
   return 1.0f / sqrtf(ss / (float)K + eps);
 }
 
-// Batch 1: stage all K columns of x into S.xs.
+// Batch 1: stage all K columns of x into S.xs as fp32 (the bf16 values,
+// widened exactly), so the MatMul loop converts only the weights.  Chunk c
+// (columns 8c .. 8c + 7) is split over two planes of float4 -- columns
+// 8c .. 8c + 3 at xs[c], 8c + 4 .. 8c + 7 at xs[nch + c] -- so that the
+// lanes of a warp read consecutive 16-byte words.
+__device__ __forceinline__ void store_f8(float4* xs, int nch, int c, uint4 v) {
+  const uint32_t* pv = &v.x;
+  float4 a, b;
+  a.x = bf_lo(pv[0]);
+  a.y = bf_hi(pv[0]);
+  a.z = bf_lo(pv[1]);
+  a.w = bf_hi(pv[1]);
+  b.x = bf_lo(pv[2]);
+  b.y = bf_hi(pv[2]);
+  b.z = bf_lo(pv[3]);
+  b.w = bf_hi(pv[3]);
+  xs[c] = a;
+  xs[nch + c] = b;
+}
+
 __device__ void stage_x_b1(const KernelParams& P, const Smem& S,
                            const TaskDesc& t, const Gemv& g) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const XSrc x = x_source(P, t);
   const int K = g.K, nch = K >> 3;
-  uint4* xs = reinterpret_cast<uint4*>(S.xs);
+  float4* xs = reinterpret_cast<float4*>(S.xs);
   if (x.mode == X_PLAIN) {
     for (int ch = tid; ch < nch; ch += kConsumers)
-      xs[ch] = __ldcg(reinterpret_cast<const uint4*>(x.a) + ch);
+      store_f8(xs, nch, ch, __ldcg(reinterpret_cast<const uint4*>(x.a) + ch));
     consumer_sync();
     return;
   }
@@ -799,7 +923,7 @@ __device__ void stage_x_b1(const KernelParams& P, const Smem& S,
   for (int k = 0; k < kMaxChunks; ++k) {
     const int ch = tid + k * kConsumers;
     if (ch < nch) {
-      xs[ch] = norm8(v[k], r, wv[k]);
+      store_f8(xs, nch, ch, norm8(v[k], r, wv[k]));
       if (x.resid) reinterpret_cast<uint4*>(x.resid)[ch] = pack8(v[k]);
     }
   }
@@ -861,26 +985,40 @@ __device__ void stage_x_seg(const KernelParams& P, const Smem& S,
 }
 
 // ------------------------------------------------------------ epilogue
-// Row results are in S.res[b * RP + page row]; write the operator's output.
+// The dot product of output row o (half 1: the up row of a gate/up tile)
+// for sequence b, from the body's result buffer: at batch 1 the sum of the
+// row's per-warp partials in a fixed order, else S.res[b * RP + page row].
+__device__ __forceinline__ float res_get(const Smem& S, const Gemv& g, int b,
+                                         int half, int o) {
+  if (g.b1) {
+    const float* q = S.res + ((size_t)half * g.rows + o) * g.wpr;
+    float v = q[0];
+    for (int s = 1; s < g.wpr; ++s) v += q[s];
+    return v;
+  }
+  const int RP = g.ngroups * kPageRows;
+  const int pr = g.dual ? 8 * (o >> 2) + 4 * half + (o & 3) : o;
+  return S.res[b * RP + pr];
+}
+
+// Write the operator's output from the row results.
 __device__ void gemv_epilogue(const KernelParams& P, const Smem& S,
                               const TaskDesc& t, const Gemv& g) {
   const Dims& D = P.dims;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int B = D.B, R = g.rows, RP = g.ngroups * kPageRows;
-  const float* res = S.res;
+  const int B = D.B, R = g.rows;
   const int l = g.layer;
   for (int idx = tid; idx < B * R; idx += kConsumers) {
     const int b = idx / R, o = idx - b * R;
     const int orow = g.row0 + o;
     if (g.dual) {
-      const int j = o >> 2, i = o & 3;
-      const float gv = round_bf(res[b * RP + 8 * j + i]);
-      const float uv = round_bf(res[b * RP + 8 * j + 4 + i]);
+      const float gv = round_bf(res_get(S, g, b, 0, o));
+      const float uv = round_bf(res_get(S, g, b, 1, o));
       lt(P, l, P.act.o_act)[(int64_t)b * g.N + orow] =
           f2bf(__fmul_rn(silu_f(gv), uv));
       continue;
     }
-    const float v = res[b * RP + o];
+    const float v = res_get(S, g, b, 0, o);
     switch (g.kind) {
       case MPK_TASK_LM_HEAD:
         P.step.logits[(int64_t)b * g.N + orow] = v;
@@ -911,11 +1049,13 @@ __device__ void gemv_epilogue(const KernelParams& P, const Smem& S,
   if (B == 1) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int o = tid; o < R; o += kConsumers)
-      if (better(res[o], g.row0 + o, bv, bi)) {
-        bv = res[o];
+    for (int o = tid; o < R; o += kConsumers) {
+      const float v = res_get(S, g, 0, 0, o);
+      if (better(v, g.row0 + o, bv, bi)) {
+        bv = v;
         bi = g.row0 + o;
       }
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float ov = __shfl_xor_sync(kFull, bv, off);
@@ -946,11 +1086,13 @@ __device__ void gemv_epilogue(const KernelParams& P, const Smem& S,
   for (int b = warp; b < B; b += kConsumerWarps) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int o = lane; o < R; o += 32)
-      if (better(res[b * RP + o], g.row0 + o, bv, bi)) {
-        bv = res[b * RP + o];
+    for (int o = lane; o < R; o += 32) {
+      const float v = res_get(S, g, b, 0, o);
+      if (better(v, g.row0 + o, bv, bi)) {
+        bv = v;
         bi = g.row0 + o;
       }
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float ov = __shfl_xor_sync(kFull, bv, off);
@@ -967,42 +1109,82 @@ __device__ void gemv_epilogue(const KernelParams& P, const Smem& S,
 }
 
 // ------------------------------------------------------------ MatMul bodies
-// Batch 1: warp w owns row w of every page; each lane reads 16-byte column
-// chunks lane, lane + 32, ... of that row and of x, four partial sums per
-// lane, one warp reduction per row.
+// Dot product of one row's chunks [c0, c1) (8 columns each) with the fp32
+// x planes (xa: first four columns of each chunk, xb: last four), one warp:
+// lane reads chunks lane, lane + 32, ...; paired fp32 FMAs (__ffma2_rn)
+// into eight independent partial sums.
+__device__ __forceinline__ void fma8(uint4 w, float4 x0, float4 x1, float2& a,
+                                     float2& b) {
+  a = __ffma2_rn(make_float2(bf_lo(w.x), bf_hi(w.x)), make_float2(x0.x, x0.y), a);
+  b = __ffma2_rn(make_float2(bf_lo(w.y), bf_hi(w.y)), make_float2(x0.z, x0.w), b);
+  a = __ffma2_rn(make_float2(bf_lo(w.z), bf_hi(w.z)), make_float2(x1.x, x1.y), a);
+  b = __ffma2_rn(make_float2(bf_lo(w.w), bf_hi(w.w)), make_float2(x1.z, x1.w), b);
+}
+__device__ __forceinline__ float row_dot(const uint4* row, const float4* xa,
+                                         const float4* xb, int c0, int c1) {
+  const int lane = threadIdx.x & 31;
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+  int ch = c0 + lane;
+  for (; ch + 32 < c1; ch += 64) {
+    fma8(row[ch], xa[ch], xb[ch], a0, a1);
+    fma8(row[ch + 32], xa[ch + 32], xb[ch + 32], a2, a3);
+  }
+  if (ch < c1) fma8(row[ch], xa[ch], xb[ch], a0, a1);
+  return warp_sum(((a0.x + a0.y) + (a1.x + a1.y)) +
+                  ((a2.x + a2.y) + (a3.x + a3.y)));
+}
+
+// Batch 1.  Flat pages: warp w dots slice w of the page (2048 elements of
+// one row).  Whole-row pages: with 8 or more rows per page warp w takes
+// rows w, w + 8, ...; with fewer, each row is split over wpr warps into
+// column ranges of equal length (multiples of 8), one partial each.
 __device__ void gemv_b1(const KernelParams& P, const Smem& S,
                         const TaskDesc& t, const Gemv& g, Ring& ring,
                         uint64_t deadline) {
   stage_x_b1(P, S, t, g);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int j = 0; j < g.ngroups; ++j) {
-    bool valid;
-    page_wrow(g, j, warp, valid);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    for (int s = 0; s < g.nsegs; ++s) {
-      const bool have = wait_full(P, S, ring, deadline);
-      if (have && valid) {
-        const int c0 = s * kSegCols, nch = min(kSegCols, g.K - c0) >> 3;
-        const uint4* row = reinterpret_cast<const uint4*>(
-            page_ptr(S, ring.slot) + warp * kPagePitch);
-        const uint4* xp = reinterpret_cast<const uint4*>(S.xs + c0);
-        if (nch == kSegCols / 8) {
-#pragma unroll
-          for (int k = 0; k < 8; k += 4) {
-            const int ch = lane + 32 * k;
-            a0 = dot8(row[ch], xp[ch], a0);
-            a1 = dot8(row[ch + 32], xp[ch + 32], a1);
-            a2 = dot8(row[ch + 64], xp[ch + 64], a2);
-            a3 = dot8(row[ch + 96], xp[ch + 96], a3);
+  const int nch = g.K >> 3;
+  const int cpw = (nch + g.wpr - 1) / g.wpr;
+  const float4* xa = reinterpret_cast<const float4*>(S.xs);
+  const float4* xb = xa + nch;
+  const int np = gemv_pages(g);
+  constexpr int kSliceChunks = kSegCols / 8;
+  for (int p = 0; p < np; ++p) {
+    int half, ne;
+    int64_t e0;
+    b1_page(g, p, half, e0, ne);
+    const bool have = wait_full(P, S, ring, deadline);
+    if (have) {
+      const uint4* pg = reinterpret_cast<const uint4*>(page_ptr(S, ring.slot));
+      float* out = S.res + (size_t)half * g.rows * g.wpr;
+      if (g.flat) {
+        const int64_t sl = e0 / kSegCols + warp;   // slice within the half
+        if (warp * kSegCols < ne) {
+          const int part = (int)(sl % g.wpr);
+          const int xo = part * kSliceChunks;
+          const float v = row_dot(pg + warp * kSliceChunks, xa + xo, xb + xo,
+                                  0, kSliceChunks);
+          if (lane == 0) out[sl] = v;
+        }
+      } else {
+        const int i0 = (int)(e0 / g.K), n = ne / g.K;
+        if (g.rpp >= kPageRows) {
+          for (int r = warp; r < n; r += kConsumerWarps) {
+            const float v = row_dot(pg + (size_t)r * nch, xa, xb, 0, nch);
+            if (lane == 0) out[i0 + r] = v;
           }
         } else {
-          for (int ch = lane; ch < nch; ch += 32) a0 = dot8(row[ch], xp[ch], a0);
+          const int r = warp / g.wpr, part = warp - r * g.wpr;
+          if (r < n) {
+            const int c0 = part * cpw;
+            const float v =
+                row_dot(pg + (size_t)r * nch, xa, xb, c0, min(nch, c0 + cpw));
+            if (lane == 0) out[(i0 + r) * g.wpr + part] = v;
+          }
         }
       }
-      release_page(S, ring, have);
     }
-    const float acc = warp_sum((a0 + a1) + (a2 + a3));
-    if (lane == 0) S.res[j * kPageRows + warp] = acc;
+    release_page(S, ring, have);
   }
   consumer_sync();
   gemv_epilogue(P, S, t, g);
@@ -1508,20 +1690,69 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
   }
   consumer_sync();
   if (!S.ctrl[4]) return;
+  // warp w merges the partials of chunks w, w + 8, ... (coalesced reads),
+  // then the 8 warp results merge as above
+  {
+    float Mw[GRP], Lw[GRP], Aw[GRP][DL];
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+      Mw[h] = -INFINITY;
+      Lw[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < DL; ++e) Aw[h][e] = 0.f;
+    }
+#pragma unroll 2
+    for (int c = warp; c < C; c += kConsumerWarps) {
+      const float* rc = part + (int64_t)c * GRP * rec;
+      float mc[GRP], lc[GRP], ac[GRP][DL];
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        mc[h] = __ldcg(rc + h * rec);
+        lc[h] = __ldcg(rc + h * rec + 1);
+#pragma unroll
+        for (int e = 0; e < DL; ++e)
+          ac[h][e] = __ldcg(rc + h * rec + 2 + lane * DL + e);
+      }
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        const float Mn = fmaxf(Mw[h], mc[h]);
+        if (Mn == -INFINITY) continue;
+        const float sa = (Mw[h] == -INFINITY) ? 0.f : expf(Mw[h] - Mn);
+        const float sc = (mc[h] == -INFINITY) ? 0.f : expf(mc[h] - Mn);
+        Lw[h] = Lw[h] * sa + lc[h] * sc;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) Aw[h][e] = Aw[h][e] * sa + ac[h][e] * sc;
+        Mw[h] = Mn;
+      }
+    }
+    consumer_sync();   // wbuf is reused
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+      float* r = wbuf + (warp * GRP + h) * rec;
+      if (lane == 0) {
+        r[0] = Mw[h];
+        r[1] = Lw[h];
+      }
+#pragma unroll
+      for (int e = 0; e < DL; ++e) r[2 + lane * DL + e] = Aw[h][e];
+    }
+    consumer_sync();
+  }
   uint16_t* out = lt(P, l, P.act.o_attn) + (int64_t)b * D.Hq * d +
                   (int64_t)g * GRP * d;
   for (int o = tid; o < GRP * d; o += kConsumers) {
     const int h = o / d, i = o - h * d;
     float M = -INFINITY;
-    for (int c = 0; c < C; ++c)
-      M = fmaxf(M, __ldcg(part + ((int64_t)c * GRP + h) * rec));
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w)
+      M = fmaxf(M, wbuf[(w * GRP + h) * rec]);
     float Ls = 0.f, A = 0.f;
-    for (int c = 0; c < C; ++c) {
-      const float* r = part + ((int64_t)c * GRP + h) * rec;
-      const float mc = __ldcg(r);
-      const float sc = (mc == -INFINITY) ? 0.f : expf(mc - M);
-      Ls = fmaf(__ldcg(r + 1), sc, Ls);
-      A = fmaf(__ldcg(r + 2 + i), sc, A);
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float* r = wbuf + (w * GRP + h) * rec;
+      const float sc = (r[0] == -INFINITY) ? 0.f : expf(r[0] - M);
+      Ls = fmaf(r[1], sc, Ls);
+      A = fmaf(r[2 + i], sc, A);
     }
     out[o] = f2bf(A / Ls);
   }
@@ -1860,9 +2091,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem S;
   if (!setup_smem(P, smem_raw, S)) return;
   const int w = blockIdx.x;
-  if ((threadIdx.x >> 5) == kConsumerWarps) {
+  const int warp = threadIdx.x >> 5;
+  if (warp >= kConsumerWarps) {
     const int a0 = P.graph.aot_off[w], a1 = P.graph.aot_off[w + 1];
-    producer_role(P, S, P.graph.aot_list + a0, a1 - a0, deadline);
+    producer_role(P, S, P.graph.aot_list + a0, a1 - a0, deadline,
+                  warp - kConsumerWarps);
   } else {
     worker_consumers(P, S, w, deadline);
   }
@@ -1877,8 +2110,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem S;
   if (!setup_smem(P, smem_raw, S)) return;
   const int task = P.graph.op_tasks[first + blockIdx.x];
-  if ((threadIdx.x >> 5) == kConsumerWarps) {
-    producer_role(P, S, P.graph.op_tasks + first + blockIdx.x, 1, deadline);
+  const int warp = threadIdx.x >> 5;
+  if (warp >= kConsumerWarps) {
+    producer_role(P, S, P.graph.op_tasks + first + blockIdx.x, 1, deadline,
+                  warp - kConsumerWarps);
   } else {
     Ring ring{0, 0};
     run_task(P, S, P.graph.tasks[task], ring, deadline);

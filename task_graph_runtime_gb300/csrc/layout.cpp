@@ -19,18 +19,20 @@ bool smem_layout(const BuiltGraph& bg, int pages_req, int limit,
   const int kmax = chain ? std::max(s.hidden, s.chain_ffn)
                          : std::max({s.hidden, s.n_q_heads * s.head_dim,
                                      s.ffn});
-  int xs = B == 1 ? round_up(kmax * 2, 16) : B * kPagePitch;
+  int xs = B == 1 ? round_up(kmax * 4, 16) : B * kPagePitch;   // fp32 x at B=1
   if (!chain) {
     const int grp = s.n_q_heads / s.n_kv_heads, d = s.head_dim;
     const int attn = (grp * d + 2 * d + 8 * grp * (2 + d)) * 4;
     xs = std::max(xs, attn);
   }
-  const int res_floats = B * (B == 1 ? 2048 : (B < 8 ? 64 : 128));
+  const int res_floats = B == 1 ? kB1Partials : B * (B < 8 ? 64 : 128);
+  const int page_bytes = B == 1 ? kContigPageBytes : kPageBytes;
   int pages = pages_req > 0 ? std::min(pages_req, 8) : 6;
   for (; pages >= 2; --pages) {
     SmemLayout L{};
     L.n_pages = pages;
-    int off = pages * kPageBytes;
+    L.page_bytes = page_bytes;
+    int off = pages * page_bytes;
     L.xs = off;
     L.xs_bytes = xs;
     off = round_up(off + xs, 128);
@@ -42,7 +44,7 @@ bool smem_layout(const BuiltGraph& bg, int pages_req, int limit,
     L.ctrl = off;
     off += 256;   // control words, 3 staged descriptors, 2 trace times
     L.scratch = off;
-    off += 1024;
+    off += 512;
     L.total = off;
     if (off <= limit) {
       *out = L;

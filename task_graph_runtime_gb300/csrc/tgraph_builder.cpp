@@ -1,6 +1,8 @@
 // Host tGraph builder.  See tgraph_builder.h for the passes and sources.
 #include "tgraph_builder.h"
 
+#include "device_abi.h"
+
 #include <algorithm>
 #include <deque>
 #include <unordered_map>
@@ -34,6 +36,7 @@ struct Decomposer {
   std::vector<BOp>& ops;
   std::vector<BTask>& tasks;
   int nl1;  // layers + 1 (tensor interning stride)
+  bool bad_rows = false;   // an explicit tile size above a tile cap
 
   int tid(int kind, int layer) const { return kind * nl1 + layer; }
 
@@ -66,8 +69,9 @@ struct Decomposer {
     begin_op(kind, layer);
     const int rpt =
         B >= 8 ? cfg.mma_rows_per_task : cfg.gemv_rows_per_task;
-    auto tl = row_tiles(n_rows, rpt, cfg.num_workers,
-                        tile_row_cap(B, dual));
+    const int cap = tile_row_cap(B, dual, k_cols);
+    if (rpt > cap) bad_rows = true;
+    auto tl = row_tiles(n_rows, rpt, cfg.num_workers, cap, B == 1 ? 1 : 8);
     for (size_t i = 0; i < tl.size(); ++i) {
       BTask& t = add_task();
       t.row0 = tl[i].first;
@@ -239,27 +243,34 @@ void fuse(std::vector<Ev>& ev) {
 
 }  // namespace
 
-int tile_row_cap(int batch, bool dual) {
-  const int page_rows = batch == 1 ? 2048 : (batch < 8 ? 64 : 128);
-  return dual ? page_rows / 2 : page_rows;
+int tile_row_cap(int batch, bool dual, int K) {
+  int rows;
+  if (batch == 1)
+    rows = kB1Partials / b1_warps_per_row(K);
+  else
+    rows = batch < 8 ? 64 : 128;
+  if (dual) rows /= 2;
+  return std::max(8, rows / 8 * 8);
 }
 
 std::vector<std::pair<int, int>> row_tiles(int n_rows, int rows_per_task,
-                                           int num_workers, int cap_rows) {
+                                           int num_workers, int cap_rows,
+                                           int unit) {
   std::vector<std::pair<int, int>> out;
   if (rows_per_task > 0) {
     for (int s = 0; s < n_rows; s += rows_per_task)
       out.emplace_back(s, std::min(n_rows, s + rows_per_task));
     return out;
   }
-  const int64_t U = (n_rows + 7) / 8;
-  const int64_t cap_u = std::max(1, cap_rows / 8);
+  const int64_t U = (n_rows + unit - 1) / unit;
+  const int64_t cap_u = std::max(1, cap_rows / unit);
   const int64_t T0 = (U + cap_u - 1) / cap_u;
   const int64_t W = std::max(1, num_workers);
   const int64_t T = std::max<int64_t>(1, std::min(U, W * ((T0 + W - 1) / W)));
   for (int64_t i = 0; i < T; ++i) {
     const int64_t u0 = (i * U) / T, u1 = ((i + 1) * U) / T;
-    out.emplace_back((int)(8 * u0), (int)std::min<int64_t>(n_rows, 8 * u1));
+    out.emplace_back((int)(unit * u0),
+                     (int)std::min<int64_t>(n_rows, unit * u1));
   }
   return out;
 }
@@ -314,9 +325,10 @@ mpk_status build_tgraph(const BuildConfig& cfg_in, BuiltGraph* out,
       cfg.mma_rows_per_task < 0 || cfg.mma_rows_per_task % 8)
     return fail(MPK_ERR_INVALID_ARG, "rows per task must be a multiple of 8");
   {
-    const int rpt = cfg.batch >= 8 ? cfg.mma_rows_per_task : cfg.gemv_rows_per_task;
-    if (rpt > tile_row_cap(cfg.batch, true))
-      return fail(MPK_ERR_UNSUPPORTED, "rows per task above the tile cap");
+    const int kmax = chain ? std::max(s.hidden, s.chain_ffn)
+                           : std::max({s.hidden, s.n_q_heads * s.head_dim, s.ffn});
+    if (kmax > 16384)
+      return fail(MPK_ERR_UNSUPPORTED, "MatMul reduction length above 16384");
   }
   if (chain) cfg.attn_chunks = 0;
   const bool attn_aot = !chain && attn_is_aot(cfg.batch, max_ctx, cfg.attn_chunks);
@@ -325,6 +337,8 @@ mpk_status build_tgraph(const BuildConfig& cfg_in, BuiltGraph* out,
   g.cfg = cfg;
   Decomposer dec{cfg, g.ops, g.tasks, s.n_layers + 1};
   dec.run();
+  if (dec.bad_rows)
+    return fail(MPK_ERR_UNSUPPORTED, "rows per task above the tile cap");
   g.n_real = (int)g.tasks.size();
   const int n_tensors = T_NKINDS * (s.n_layers + 1);
 

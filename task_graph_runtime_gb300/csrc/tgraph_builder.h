@@ -56,17 +56,20 @@ struct BuiltGraph {
   int root_lin = 0, end_lin = 0;   // linear ids of the root and end events
 };
 
-// Most output rows one MatMul tile may hold: its weight pages' rows land in
-// a per-tile result buffer and, at batch > 1, in per-thread accumulators.
-// Page rows: 2048 at batch 1, 64 at batch 2..7, 128 at batch >= 8; a
-// gate/up tile holds two page rows per output row.
-int tile_row_cap(int batch, bool dual);
+// Most output rows one MatMul tile with reduction length K may hold.  Batch
+// 1: its row partial sums (rows x warps per row, twice for a gate/up tile)
+// fit the 2560-float result buffer; batch 2..7: 64 weight rows, batch >= 8:
+// 128 weight rows (per-thread accumulators); a gate/up tile streams two
+// weight rows per output row.  Rounded down to a multiple of 8.
+int tile_row_cap(int batch, bool dual, int K);
 
-// Row tiling of an N-row MatMul: explicit size (a multiple of 8, at most the
-// cap), or T = W * ceil(T0 / W) tiles (at most U = ceil(N/8)) with
-// T0 = ceil(U / (cap/8)), boundaries at 8 * floor(i*U/T) rows.
+// Row tiling of an N-row MatMul in units of `unit` rows (1 at batch 1, 8
+// otherwise): explicit size (at most the cap), or T = W * ceil(T0 / W)
+// tiles (at most U = ceil(N/unit)) with T0 = ceil(U / (cap/unit)),
+// boundaries at unit * floor(i*U/T) rows.
 std::vector<std::pair<int, int>> row_tiles(int n_rows, int rows_per_task,
-                                           int num_workers, int cap_rows);
+                                           int num_workers, int cap_rows,
+                                           int unit);
 
 // Attention chunks are AOT (their KV prefetched into the ring) at batch 1
 // when no chunk can exceed 128 tokens, JIT otherwise.

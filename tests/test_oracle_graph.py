@@ -213,29 +213,34 @@ def test_launch_classes_and_aot_round_robin(built):
 
 
 def test_row_tiles_cover_rows():
-    """Default tiles: contiguous, multiples of 8 rows, within the cap, a
-    multiple of W of them unless every tile is one 8-row unit, sizes within
-    one unit of each other."""
-    for n in (8, 64, 688, 1000, 6144, 12288, 151936):
-        for W in (1, 7, 148):
-            for cap in (32, 64, 128, 1024, 2048):
-                tl = tgraph.row_tiles(n, 0, W, cap)
-                assert tl[0][0] == 0 and tl[-1][1] == n
-                assert all(a[1] == b[0] for a, b in zip(tl, tl[1:]))
-                assert all(r0 % 8 == 0 and r1 > r0 for r0, r1 in tl)
-                assert all(r1 - r0 <= cap for r0, r1 in tl)
-                U = -(-n // 8)
-                assert len(tl) % W == 0 or len(tl) == U
-                sizes = [r1 - r0 for r0, r1 in tl[:-1]]
-                if sizes:
-                    assert max(sizes) - min(sizes) <= 8
+    """Default tiles: contiguous, multiples of the unit, within the cap, a
+    multiple of W of them unless every tile is one unit, sizes within one
+    unit of each other."""
+    for unit in (1, 8):
+        for n in (8, 64, 688, 1000, 6144, 12288, 151936):
+            for W in (1, 7, 148):
+                for cap in (32, 64, 128, 1024, 2048):
+                    tl = tgraph.row_tiles(n, 0, W, cap, unit)
+                    assert tl[0][0] == 0 and tl[-1][1] == n
+                    assert all(a[1] == b[0] for a, b in zip(tl, tl[1:]))
+                    assert all(r0 % unit == 0 and r1 > r0 for r0, r1 in tl)
+                    assert all(r1 - r0 <= cap for r0, r1 in tl)
+                    U = -(-n // unit)
+                    assert len(tl) % W == 0 or len(tl) == U
+                    sizes = [r1 - r0 for r0, r1 in tl[:-1]]
+                    if sizes:
+                        assert max(sizes) - min(sizes) <= unit
 
 
 def test_tile_caps_by_batch():
-    assert tgraph.tile_row_cap(1, False) == 2048
-    assert tgraph.tile_row_cap(1, True) == 1024
-    assert tgraph.tile_row_cap(4, False) == 64
-    assert tgraph.tile_row_cap(16, True) == 64
+    assert tgraph.tile_row_cap(1, False, 4096) == 1280     # 4 rows/page, 2 warps/row
+    assert tgraph.tile_row_cap(1, True, 4096) == 640
+    assert tgraph.tile_row_cap(1, False, 12288) == 424     # 6 slices/row
+    assert tgraph.tile_row_cap(1, False, 688) == 2560      # 23 rows/page
+    assert tgraph.tile_row_cap(1, False, 2048) == 2560     # 8 rows/page
+    assert tgraph.tile_row_cap(1, False, 256) == 2560
+    assert tgraph.tile_row_cap(4, False, 4096) == 64
+    assert tgraph.tile_row_cap(16, True, 12288) == 64
 
 
 def test_coarse_events_are_operator_level():
