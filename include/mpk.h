@@ -255,11 +255,14 @@ mpk_status mpk_debug_add_event_count(mpk_graph* g, int event, int delta);
 
 /* Tracing (megakernel mode).  mpk_debug_set_trace(g, capacity) allocates
  * room for `capacity` task records (0 disables).  Each executed task adds one
- * record of four uint64: task id | (worker << 32), and the %globaltimer
+ * record of eight uint64: task id | (worker << 32), then the %globaltimer
  * nanoseconds at which the worker's leader started looking for it, found it
- * ready and finished it (after its trigger).  mpk_debug_read_trace copies up
- * to `capacity` records into host_records, stores the count, and clears the
- * trace for the next steps (synchronises the device). */
+ * ready, had its operands staged (batch-1 MatMul tiles; else 0), had
+ * consumed its last weight page (batch-1 MatMul tiles; else 0), finished its
+ * body, and finished its trigger; the eighth word is 0.
+ * mpk_debug_read_trace copies up to `capacity` records into host_records,
+ * stores the count, and clears the trace for the next steps (synchronises
+ * the device). */
 mpk_status mpk_debug_set_trace(mpk_graph* g, int capacity);
 mpk_status mpk_debug_read_trace(mpk_graph* g, uint64_t* host_records,
                                 int capacity, int* n_records);

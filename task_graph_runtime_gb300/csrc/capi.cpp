@@ -69,7 +69,7 @@ void fill_export(mpk_graph* g) {
 
 // Fixed-size descriptors in linear order; per-worker AOT lists; per-op task
 // lists for the kernel-per-operator mode.
-void encode(mpk_graph* g) {
+bool encode(mpk_graph* g) {
   const BuiltGraph& bg = g->bg;
   const int nT = (int)bg.order.size(), nE = (int)bg.ev_count.size();
   const int W = bg.cfg.num_workers;
@@ -99,10 +99,15 @@ void encode(mpk_graph* g) {
     d.first = bg.ev_first[e];
     d.last = bg.ev_last[e];
     d.flags = 0;
+    uint32_t n_inline = 0;
     for (int p = d.first; p <= d.last; ++p) {
       if (bg.launch[p] == MPK_LAUNCH_JIT) d.flags |= EV_HAS_JIT;
-      if (bg.launch[p] == MPK_LAUNCH_INLINE) d.flags |= EV_HAS_INLINE;
+      if (bg.launch[p] == MPK_LAUNCH_INLINE) {
+        d.flags |= EV_HAS_INLINE;
+        ++n_inline;
+      }
     }
+    d.flags |= n_inline << kEvInlineShift;
   }
   std::vector<std::vector<int32_t>> lists(W);
   for (int p = 0; p < nT; ++p)
@@ -120,7 +125,16 @@ void encode(mpk_graph* g) {
     g->h_op_first.push_back((int32_t)g->h_op_tasks.size());
     for (int i = 0; i < o.n; ++i) g->h_op_tasks.push_back(pos_of[o.first + i]);
   }
+  // inline tasks must be the suffix of each event's range (see
+  // kEvInlineShift); the builder's numbering guarantees it
+  for (int e = 0; e < nE; ++e) {
+    const EventDesc& d = g->h_events[e];
+    const int n_in = (int)(d.flags >> kEvInlineShift);
+    for (int p = d.last - n_in + 1; p <= d.last; ++p)
+      if (bg.launch[p] != MPK_LAUNCH_INLINE) return false;
+  }
   g->encoded = true;
+  return true;
 }
 
 }  // namespace
@@ -190,7 +204,7 @@ mpk_status mpk_build_tgraph(const mpk_model_shape* shape,
     if (ms > 0) g->timeout_ns = (uint64_t)ms * 1000000ull;
   }
   fill_export(g.get());
-  encode(g.get());
+  if (!encode(g.get())) return MPK_ERR_GRAPH_INVALID;
   *out = g.release();
   return MPK_OK;
 }
@@ -493,7 +507,7 @@ mpk_status mpk_debug_set_trace(mpk_graph* g, int capacity) {
   g->params.graph.trace_count = nullptr;
   g->params.graph.trace_cap = 0;
   if (capacity == 0) return MPK_OK;
-  CK(g->d_trace.alloc((size_t)capacity * 4));
+  CK(g->d_trace.alloc((size_t)capacity * 8));
   CK(g->d_trace_count.alloc(1));
   CK(cudaMemset(g->d_trace_count.p, 0, sizeof(uint32_t)));
   g->params.graph.trace = g->d_trace.p;
@@ -512,7 +526,7 @@ mpk_status mpk_debug_read_trace(mpk_graph* g, uint64_t* host_records,
   if (n > g->params.graph.trace_cap) n = g->params.graph.trace_cap;
   const int take = (int)n < capacity ? (int)n : capacity;
   if (take > 0 && host_records)
-    CK(cudaMemcpy(host_records, g->d_trace.p, (size_t)take * 32,
+    CK(cudaMemcpy(host_records, g->d_trace.p, (size_t)take * 64,
                   cudaMemcpyDeviceToHost));
   CK(cudaMemset(g->d_trace_count.p, 0, sizeof(uint32_t)));
   *n_records = take;

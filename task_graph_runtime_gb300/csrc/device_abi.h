@@ -30,7 +30,11 @@ static_assert(sizeof(TaskDesc) == 32, "task descriptor must stay 32 bytes");
 // Tile 0 of a MatMul whose prologue forms a residual sum also stores it.
 enum : uint8_t { TASK_F_RESIDUAL = 1u };
 
+// Event flags.  Empty (inline) tasks get the highest ids and BFS appends
+// an event's dependent tasks in ascending id, so an event's inline tasks are
+// the last n of [first, last]; n is stored in bits 8..31.
 enum : uint32_t { EV_HAS_JIT = 1u, EV_HAS_INLINE = 2u };
+constexpr int kEvInlineShift = 8;
 
 // 16-byte event descriptor: activated when its counter reaches
 // epoch * count; its dependent tasks are [first, last].

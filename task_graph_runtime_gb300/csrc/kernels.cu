@@ -249,9 +249,11 @@ struct Smem {
   uint64_t* full;
   uint64_t* empty;
   volatile int* ctrl; // [0..1] command, [2] bail-out, [3] aborted at entry,
-                      // [4] last-chunk flag
+                      // [4] last-chunk flag, [5] leader polling an event,
+                      // [8..10] leader loop state
   TaskDesc* desc;     // [0..1] staged descriptors, [2] the head AOT task's
-  uint64_t* times;    // [2] trace: looked-for, ready
+  uint64_t* times;    // trace: [0] looked-for, [1] ready, [2] operands
+                      // staged, [3] last page consumed, [4] body done
   float* scratch;
   int n_pages;
   int page_bytes;
@@ -271,6 +273,12 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const SmemLayout& L) {
   s.n_pages = L.n_pages;
   s.page_bytes = L.page_bytes;
   return s;
+}
+
+// Trace stamp `i` (thread 0, tracing on only).
+__device__ __forceinline__ void stamp(const KernelParams& P, const Smem& S,
+                                      int i) {
+  if (P.graph.trace && threadIdx.x == 0) S.times[i] = globaltimer();
 }
 
 // Position in the ring of pages, advanced identically by the producer and
@@ -638,7 +646,7 @@ __device__ bool la_step(const KernelParams& P, const int32_t* list, int n,
       la.p = 0;
     }
     if (la.p < la.np) {
-      if (prefetch && la.gemv) prefetch_gemv_page(la.g, la.p);
+      if (prefetch && la.gemv && la.g.b1) prefetch_gemv_page(la.g, la.p);
       ++la.p;
       ++la.count;
       return true;
@@ -649,28 +657,39 @@ __device__ bool la_step(const KernelParams& P, const int32_t* list, int n,
   return false;
 }
 
-// While the consumers hold every ring page and everything issued has
-// landed -- they are waiting for an event, not for data -- prefetch the
-// next pages into L2, up to `pf` pages beyond the ring, so HBM keeps
-// streaming during the wait.  In steady streaming the newest page is still
-// in flight and nothing is prefetched.
-__device__ void prefetch_while_idle(const KernelParams& P, const Smem& S,
-                                    const int32_t* list, int n, Lookahead& la,
-                                    const Ring& ring, int last_slot,
-                                    uint32_t last_phase, int64_t copied,
-                                    int pf) {
+// Bounded wait for a free ring slot (lane 0 spins, the other lanes then
+// observe the phase).  While it waits and the consumers' leader is polling
+// for an event (S.ctrl[5], set around the poll), the HBM stream of this SM
+// would stop; instead lane 0 prefetches the next batch-1 weight pages into
+// L2 (cp.async.bulk.prefetch.L2), up to `pf` pages beyond page `gp`, so the
+// copies after the event hit L2.  In steady streaming the leader is running
+// a task, and nothing is prefetched.
+__device__ bool wait_empty_pf(const KernelParams& P, const Smem& S,
+                              const Ring& ring, uint64_t deadline, int pf,
+                              Lookahead& la, const int32_t* list, int n,
+                              int64_t gp) {
   const int lane = threadIdx.x & 31;
-  while (la.count < copied)
-    if (!la_step(P, list, n, la, false)) return;
-  while (la.count < copied + pf) {
-    int idle = 0;
-    if (lane == 0)
-      idle = !mbar_test(&S.empty[ring.slot], ring.phase ^ 1u) &&
-             (last_slot < 0 || mbar_test(&S.full[last_slot], last_phase)) &&
-             !aborted(P);
-    if (!__shfl_sync(kFull, idle, 0)) return;
-    if (!la_step(P, list, n, la, true)) return;
+  int ok = 1;
+  if (lane == 0) {
+    uint32_t spins = 0;
+    while (!mbar_try_wait(&S.empty[ring.slot], ring.phase ^ 1u)) {
+      if (pf > 0 && S.ctrl[5]) {
+        while (la.count < gp)
+          if (!la_step(P, list, n, la, false)) break;
+        if (la.count < gp + pf && la.i < n) la_step(P, list, n, la, true);
+      }
+      if ((++spins & 1023u) == 0u &&
+          (aborted(P) || globaltimer() > deadline)) {
+        if (!aborted(P)) raise_error(P, MPK_ERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+    }
+    if (ok && aborted(P)) ok = 0;
   }
+  ok = __shfl_sync(kFull, ok, 0);
+  if (ok) (void)mbar_try_wait(&S.empty[ring.slot], ring.phase ^ 1u);
+  return ok != 0;
 }
 
 // Producer warp `pid` of kProducerWarps: walks the task list and issues
@@ -692,8 +711,6 @@ __device__ void producer_role(const KernelParams& P, const Smem& S,
   Lookahead la{0, 0, -1, 0, Gemv{}, false};
   Ring ring{0, 0};
   int64_t gp = 0;
-  int last_slot = -1;
-  uint32_t last_phase = 0;
   int turn = 0;            // gp % 2
   for (int i = 0; i < n; ++i) {
     const TaskDesc t = P.graph.tasks[list[i]];
@@ -719,10 +736,7 @@ __device__ void producer_role(const KernelParams& P, const Smem& S,
         }
       }
       if (!mine) continue;
-      if (pf > 0)
-        prefetch_while_idle(P, S, list, n, la, ring, last_slot, last_phase,
-                            gp, pf);
-      if (!wait_empty(P, S, ring, deadline)) {
+      if (!wait_empty_pf(P, S, ring, deadline, pf, la, list, n, gp)) {
         drain_copies(P, S, issued);
         return;
       }
@@ -743,8 +757,6 @@ __device__ void producer_role(const KernelParams& P, const Smem& S,
       }
       __syncwarp();
       issued[ring.slot] = 1u | (ring.phase << 1);
-      last_slot = (int)ring.slot;
-      last_phase = ring.phase;
     }
   }
   // the consumers wait for every page before leaving, so all copies have
@@ -815,6 +827,19 @@ __device__ XSrc x_source(const KernelParams& P, const TaskDesc& t) {
       break;
   }
   return x;
+}
+
+// Prefetch into L2 the RMSNorm gain of a MatMul task's prologue (a weight,
+// independent of any event), so the prologue after the event finds it
+// there.  One thread.
+__device__ __forceinline__ void prefetch_gain(const KernelParams& P,
+                                              const TaskDesc& t) {
+  if (!is_gemv(t.kind)) return;
+  const XSrc x = x_source(P, t);
+  if (x.mode == X_PLAIN) return;
+  const char* p = reinterpret_cast<const char*>(x.gain);
+  for (int off = 0; off < P.dims.h * 2; off += 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off) : "memory");
 }
 
 // Pre-norm values of 8 columns [k, k + 8) of sequence b.
@@ -1142,6 +1167,7 @@ __device__ void gemv_b1(const KernelParams& P, const Smem& S,
                         const TaskDesc& t, const Gemv& g, Ring& ring,
                         uint64_t deadline) {
   stage_x_b1(P, S, t, g);
+  stamp(P, S, 2);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nch = g.K >> 3;
   const int cpw = (nch + g.wpr - 1) / g.wpr;
@@ -1187,6 +1213,7 @@ __device__ void gemv_b1(const KernelParams& P, const Smem& S,
     release_page(S, ring, have);
   }
   consumer_sync();
+  stamp(P, S, 3);
   gemv_epilogue(P, S, t, g);
 }
 
@@ -1558,13 +1585,13 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
     if (!pre) __threadfence();   // the new K/V row is read back below
     consumer_sync();
   }
+  stamp(P, S, 2);
   float qr[GRP][DL];
 #pragma unroll
   for (int h = 0; h < GRP; ++h)
 #pragma unroll
     for (int e = 0; e < DL; ++e) qr[h][e] = qf[h * d + lane * DL + e];
   // ---- online softmax over this warp's token blocks
-  const int my_h = lane % GRP;
   float m_run = -INFINITY, l_run = 0.f;
   float acc[GRP][DL];
 #pragma unroll
@@ -1631,6 +1658,7 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
       }
     }
   }
+  stamp(P, S, 3);
   if (pre) {
     // the pages were written through the generic proxy (new token): order
     // that before the producer's next bulk copy into them
@@ -1903,8 +1931,8 @@ __device__ void trigger(const KernelParams& P, int e, uint64_t deadline) {
         return;
     }
     if (ed.flags & EV_HAS_INLINE) {
-      for (int t = ed.first; t <= ed.last; ++t) {
-        if (G.tasks[t].launch != MPK_LAUNCH_INLINE) continue;
+      const int n_in = (int)(ed.flags >> kEvInlineShift);
+      for (int t = ed.last - n_in + 1; t <= ed.last; ++t) {
         if (sp >= 16) {
           raise_error(P, MPK_ERR_QUEUE_OVERFLOW);
           return;
@@ -1921,24 +1949,26 @@ __device__ __forceinline__ bool event_done(const KernelParams& P, int e) {
 }
 
 // ------------------------------------------------------------ roles
+// Leader-only loop state lives in shared memory (S.ctrl[8..10]) rather than
+// in registers that every thread would carry across the task bodies.
 __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
                                  uint64_t deadline) {
   const DevGraph& G = P.graph;
   const int tid = threadIdx.x;
-  const int a0 = G.aot_off[w], a1 = G.aot_off[w + 1];
-  int ai = a0;
-  uint32_t jit_head = 0;
-  RingHdr* jh = G.jit_hdr + w;
-  uint64_t* js = G.jit_slots + (size_t)w * G.jit_cap;
+  volatile int* ai_s = S.ctrl + 8;        // next AOT list position
+  volatile int* head_s = S.ctrl + 9;      // its task id, -1 past the end
+  volatile int* jit_s = S.ctrl + 10;      // JIT ring head
   // The head AOT task's descriptor is prefetched into shared memory as soon
   // as the task before it is dispatched, before its event is polled.
   TaskDesc* head = &S.desc[2];
-  int head_id = -1;
   if (tid == 0) {
-    jit_head = ld_relaxed(&jh->head);
-    if (ai < a1) {
-      head_id = G.aot_list[ai];
-      *head = G.tasks[head_id];
+    const int a0 = G.aot_off[w], a1 = G.aot_off[w + 1];
+    *jit_s = (int)ld_relaxed(&G.jit_hdr[w].head);
+    *ai_s = a0;
+    *head_s = -1;
+    if (a0 < a1) {
+      *head_s = G.aot_list[a0];
+      *head = G.tasks[*head_s];
     }
   }
   Ring ring{0, 0};
@@ -1946,9 +1976,16 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
   while (true) {
     if (tid == 0) {
       if (G.trace) S.times[0] = globaltimer();
+      int head_id = *head_s;
+      // warm L2 with the head task's weight-side prologue operand
+      if (head_id >= 0) prefetch_gain(P, *head);
+      RingHdr* jh = G.jit_hdr + w;
+      uint64_t* js = G.jit_slots + (size_t)w * G.jit_cap;
+      uint32_t jit_head = (uint32_t)*jit_s;
       int cmd = -1;
       uint32_t spins = 0;
       const int head_dep = (head_id >= 0) ? head->dep : G.end;
+      S.ctrl[5] = 1;   // waiting on an event: the producers may prefetch
       while (!S.ctrl[2]) {
         uint32_t v;
         if (ring_try_pop(jh, js, G.jit_cap, jit_head, v)) {
@@ -1960,8 +1997,10 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
           cmd = head_id;   // -1 when the end event fired
           if (head_id >= 0) {
             S.desc[iter & 1] = *head;
-            ++ai;
-            head_id = (ai < a1) ? G.aot_list[ai] : -1;
+            const int ai = *ai_s + 1;
+            *ai_s = ai;
+            head_id = (ai < G.aot_off[w + 1]) ? G.aot_list[ai] : -1;
+            *head_s = head_id;
             if (head_id >= 0) *head = G.tasks[head_id];
           }
           break;
@@ -1976,8 +2015,13 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
           }
         }
       }
+      S.ctrl[5] = 0;
+      *jit_s = (int)jit_head;
       fence_acq_rel_gpu();
-      if (G.trace) S.times[1] = globaltimer();
+      if (G.trace) {
+        S.times[1] = globaltimer();
+        S.times[2] = S.times[3] = 0;
+      }
       S.ctrl[iter & 1] = cmd;
     }
     consumer_sync();
@@ -1987,20 +2031,28 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
     if (cmd < 0) break;
     run_task(P, S, S.desc[slot], ring, deadline);
     consumer_sync();
+    stamp(P, S, 4);
     // only the leader decides to stop (at its next poll), so all consumer
     // threads leave through the same broadcast
     if (tid == 0 && !S.ctrl[2] && !aborted(P)) {
-      __threadfence();
+      // the red.release / atom.acq_rel of the trigger is cumulative: it
+      // orders every write of the CTA that the barrier above ordered before
+      // this thread
       trigger(P, S.desc[slot].trig, deadline);
       if (G.trace) {
-        // (task | worker << 32), looked-for, ready, done
+        // (task | worker << 32), looked-for, ready, staged, pages done,
+        // body done, triggered
         const uint32_t k = atomicAdd(G.trace_count, 1u);
         if (k < G.trace_cap) {
-          uint64_t* r = G.trace + 4ull * k;
+          uint64_t* r = G.trace + 8ull * k;
           r[0] = (uint64_t)(uint32_t)cmd | ((uint64_t)(uint32_t)w << 32);
           r[1] = S.times[0];
           r[2] = S.times[1];
-          r[3] = globaltimer();
+          r[3] = S.times[2];
+          r[4] = S.times[3];
+          r[5] = S.times[4];
+          r[6] = globaltimer();
+          r[7] = 0;
         }
       }
     }
@@ -2070,6 +2122,7 @@ __device__ __forceinline__ bool setup_smem(const KernelParams& P, uint8_t* raw,
     // mpk_reset; read it once per CTA so all threads agree
     S.ctrl[3] = aborted(P) ? 1 : 0;
     S.ctrl[4] = 0;
+    S.ctrl[5] = 0;
     fence_proxy_async_smem();
   }
   __syncthreads();

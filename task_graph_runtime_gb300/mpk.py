@@ -299,8 +299,9 @@ class Graph:
                "mpk_debug_set_trace")
 
     def read_trace(self, capacity: int) -> np.ndarray:
-        """uint64 [n, 4]: task | worker << 32, looked, ready, done (ns)."""
-        buf = np.zeros((capacity, 4), np.uint64)
+        """uint64 [n, 8]: task | worker << 32, looked, ready, staged, pages
+        done, body done, triggered (ns; 0 where not recorded), 0."""
+        buf = np.zeros((capacity, 8), np.uint64)
         n = ctypes.c_int(0)
         _check(load_library().mpk_debug_read_trace(
             self.handle, buf.ctypes.data, capacity, ctypes.byref(n)),
