@@ -207,19 +207,22 @@ class OracleSample:
                        f"lm_head rows, scaled x{s.n_layers}")
 
     def run_once(self) -> float:
-        """Seconds of one sample (already scaled to a whole step)."""
+        """Seconds of one sample, scaled to a whole step (the unscaled
+        wall time is left in ``self.last_raw``)."""
         nx = self.nx
         t = time.perf_counter()
         if self.wl.shape.is_chain:
             toks = np.zeros(self.B, np.int32)
             nx.decode_step(self.wl.shape, self.W, toks, None, None, None, None)
-            return time.perf_counter() - t
+            self.last_raw = time.perf_counter() - t
+            return self.last_raw
         seq = self.kv.seq_lens.copy()
         h = nx.layer_step(self.one, self.W, 0, self.x, self.kv.k_pool,
                           self.kv.v_pool, self.kv.page_table, seq)
         nf = nx.rmsnorm(h, self.W["layer0.ln1"], self.one.rms_eps)
         nx.argmax_lowest(nx.linear(nf, self.lm))
-        return (time.perf_counter() - t) * self.scale
+        self.last_raw = time.perf_counter() - t
+        return self.last_raw * self.scale
 
 
 def cpu_baseline(wl, budget_s: float = 12.0) -> dict:
@@ -270,10 +273,22 @@ def run_ours(args, rank, world, local_rank):
     ex = g.export()
     n_launch_per_step = 1 if mode == mpk.MODE_MEGAKERNEL else ex["n_ops"]
 
-    def step(i):
+    def rewind(i):
         if kv is not None and i % block == 0:
             kv.seq_lens.copy_(seq0, non_blocking=True)
-        g.decode_step(toks[i % 2], kv, logits, toks[(i + 1) % 2], stream)
+
+    def launch(i, m):
+        if m == mpk.MODE_KPO_GRAPH:
+            # a captured graph replays fixed buffers: feed the next token
+            # back with a 4-byte-per-sequence device copy
+            g.decode_step(toks[0], kv, logits, toks[1], stream)
+            toks[0].copy_(toks[1], non_blocking=True)
+        else:
+            g.decode_step(toks[i % 2], kv, logits, toks[(i + 1) % 2], stream)
+
+    def step(i):
+        rewind(i)
+        launch(i, mode)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -295,8 +310,9 @@ def run_ours(args, rank, world, local_rank):
         time.sleep(0.3)
         start.record(stream)
         for i in range(args.steps):
+            rewind(i)
             ev[i][0].record(stream)
-            step(i)
+            launch(i, mode)
             ev[i][1].record(stream)
         end.record(stream)
         torch.cuda.synchronize(dev)
@@ -329,6 +345,37 @@ def run_ours(args, rank, world, local_rank):
             stream.synchronize()
             h_tok.copy_(h_next)
         e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+
+    # the same task bodies launched kernel-per-operator (plain, and replayed
+    # from a CUDA Graph), same process and inputs: the comparison point
+    compare = {}
+    if args.compare and world == 1:
+        n_cmp = max(4, min(args.steps, 2 * block))
+        for name, m in (("megakernel", mpk.MODE_MEGAKERNEL),
+                        ("kpo", mpk.MODE_KPO),
+                        ("kpo_graph", mpk.MODE_KPO_GRAPH)):
+            if m == mode:
+                continue
+            g.set_mode(m)
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    rewind(i)
+                    launch(i, m)
+                torch.cuda.synchronize(dev)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for i in range(n_cmp):
+                    rewind(i)
+                    launch(i, m)
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+            if g.status() != mpk.MPK_OK:
+                raise RuntimeError(f"{name} steps failed")
+            compare[name] = {"ms_per_step": round(a.elapsed_time(b) / n_cmp,
+                                                  5),
+                             "steps": n_cmp}
+        g.set_mode(mode)
     g.close()
 
     # byte model over one rewind block of steps
@@ -382,6 +429,7 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": 4 * B, "d2h_bytes_per_step": 4 * B,
                 "steps": e2e_steps},
         "gpu_launches": args.steps * n_launch_per_step,
+        "same_run_modes": compare,
         "graph": {"tasks": ex["n_tasks"], "events": ex["n_events"],
                   "empty_tasks": ex["n_empty"], "workers": ex["n_workers"],
                   "attn_chunks": ex["attn_chunks"]},
@@ -409,12 +457,19 @@ def run_reference(args):
     smp = OracleSample(wl)
     for _ in range(args.warmup):
         smp.run_once()
-    t = [smp.run_once() for _ in range(args.steps)]
+    t, raw = [], []
+    for _ in range(args.steps):
+        t.append(smp.run_once())
+        raw.append(smp.last_raw)
     v = statistics.mean(t) * 1e3 / wl.batch
     cores = _blas_threads()
+    # each step runs the bounded sample; ms_per_step is its wall time, and
+    # `value` scales it to a whole step of the workload (see `sample`)
     return {"impl": "reference", "metric": METRIC, "value": round(v, 3),
             "unit": "ms/token", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(v * wl.batch, 3),
+            "warmup": args.warmup,
+            "ms_per_step": round(statistics.mean(raw) * 1e3, 3),
+            "sample_scale": smp.scale,
             "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded random bf16 weights and KV cache)",
@@ -438,6 +493,8 @@ def main():
     ap.add_argument("--mode", default="mega",
                     choices=["mega", "kpo", "kpo_graph"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-compare", dest="compare", action="store_false",
+                    help="skip the same-run kernel-per-operator timings")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

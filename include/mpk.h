@@ -90,10 +90,6 @@ typedef struct {
   int sched_warps_per_sm; /* 0: 4 (Table 1)                                 */
   int smem_pages;         /* weight pages (8 rows x 2048 columns, 32 KB +
                              row skew) per worker. 0: as many as fit, <= 6  */
-  int l2_prefetch_pages;  /* pages each worker may prefetch into L2 beyond
-                             its shared-memory ring while its consumers
-                             wait on an event (cp.async.bulk.prefetch).
-                             <= 0: none (the default)                       */
   int coarse_events;      /* 1: every task of an operator waits for every
                              task of the operators it reads (the
                              operator-level graph of Figure 4c, an

@@ -198,7 +198,6 @@ mpk_status mpk_build_tgraph(const mpk_model_shape* shape,
   g->sched_warps_per_sm = sched_warps;
   if (t.smem_pages < 0 || t.smem_pages > 8) return MPK_ERR_INVALID_ARG;
   g->pages_req = t.smem_pages;
-  g->pf_pages = t.l2_prefetch_pages > 0 ? t.l2_prefetch_pages : kDefaultPfPages;
   if (const char* env = std::getenv("MPK_WAIT_TIMEOUT_MS")) {
     const long ms = std::strtol(env, nullptr, 10);
     if (ms > 0) g->timeout_ns = (uint64_t)ms * 1000000ull;
@@ -322,7 +321,7 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
 
   KernelParams& P = g->params;
   P = KernelParams{};
-  P.dims = make_dims(g->bg, g->pf_pages);
+  P.dims = make_dims(g->bg);
   P.sm = sm;
   DevGraph& G = P.graph;
   G.tasks = g->d_tasks.p;

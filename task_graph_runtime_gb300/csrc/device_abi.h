@@ -116,7 +116,6 @@ struct Dims {
   int n_lm_tiles;
   int max_ctx;       // rows of the RoPE table
   int kmax;          // longest MatMul reduction (x staging at batch 1)
-  int pf_pages;      // weight pages prefetched into L2 ahead of the ring
 };
 
 // Activation workspace: one block per layer (identical layout), plus a
@@ -146,7 +145,7 @@ struct DevGraph {
   uint32_t jit_cap, sched_cap;
   uint32_t* status;            // latched mpk_status
   uint32_t* abort_flag;
-  uint64_t* trace;             // nullable: 4 words per executed task
+  uint64_t* trace;             // nullable: 8 words per executed task
   uint32_t* trace_count;
   uint32_t trace_cap;          // records
   int W;                       // worker CTAs

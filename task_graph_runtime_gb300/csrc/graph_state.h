@@ -14,7 +14,6 @@ namespace mpk_detail {
 
 constexpr uint32_t kJitCap = 1024;
 constexpr uint32_t kSchedCap = 4096;
-constexpr int kDefaultPfPages = 0;
 constexpr int kSmemLimit = 232448;   // 227 KB per block on sm_100-class
 
 template <typename T>
@@ -48,8 +47,7 @@ using mpk_detail::DevBuf;
 struct mpk_graph {
   mpk::BuiltGraph bg;
   uint64_t uid = 0;   // build number, unique within the process
-  int num_sched_sms = 4, sched_warps_per_sm = 4, pages_req = 0,
-      pf_pages = mpk_detail::kDefaultPfPages;
+  int num_sched_sms = 4, sched_warps_per_sm = 4, pages_req = 0;
   // export arrays (linear order)
   std::vector<int32_t> x_kind, x_op, x_layer, x_tile, x_row0, x_row1, x_b,
       x_g, x_c, x_pre, op_kind, op_layer, op_n;

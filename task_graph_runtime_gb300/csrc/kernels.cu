@@ -13,16 +13,14 @@
 //     (and the KV cache of earlier tokens) never depend on an event;
 //   "关键实现细节" 2 -- task descriptors prefetched before dequeue.
 //
-// GB300 layout of a worker CTA (one per SM, 320 threads):
+// GB300 layout of a worker CTA (one per SM, 384 threads = 3 warpgroups):
 //   warps 8, 9  -- producers: both walk this worker's AOT task list and
 //                  take alternate pages of it (two independent bulk-copy
 //                  streams per SM sustain more HBM bandwidth than one).
 //                  Weight pages arrive by 1-D bulk copies (cp.async.bulk):
 //                  one contiguous copy of up to 32 KB at batch 1, one per
 //                  matrix row at batch > 1; AOT attention tasks get their
-//                  KV chunk the same way.  Optionally a look-ahead cursor
-//                  prefetches pages into L2 (cp.async.bulk.prefetch.L2)
-//                  while the consumers wait on an event;
+//                  KV chunk the same way;
 //   warps 0..7  -- consumers: poll events and the JIT queue, run task bodies,
 //                  release pages, trigger events.
 // MatMul tiles run on CUDA cores at batch < 8 and on tensor cores
@@ -42,7 +40,16 @@ namespace mpk {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarps = 2;   // two bulk-copy streams per SM
-constexpr int kThreads = kConsumers + 32 * kProducerWarps;
+// Three warpgroups: two of consumers, one holding the producers (its other
+// two warps only take part in the register hand-over and leave).  Launched
+// at kLaunchRegs registers a thread; the producer warpgroup gives registers
+// back (setmaxnreg.dec) and the consumer warpgroups take them: 256 * 216 +
+// 128 * 72 = 384 * 168.
+constexpr int kThreads = kConsumers + 128;
+constexpr int kLaunchRegs = 168, kConsumerRegs = 216, kProducerRegs = 72;
+static_assert(kConsumers * kConsumerRegs + 128 * kProducerRegs <=
+                  kThreads * kLaunchRegs,
+              "register hand-over must fit the launch allocation");
 constexpr int kMaxRingPages = 8;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -103,11 +110,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src,
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src),
-               "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
@@ -165,6 +167,14 @@ __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -249,8 +259,7 @@ struct Smem {
   uint64_t* full;
   uint64_t* empty;
   volatile int* ctrl; // [0..1] command, [2] bail-out, [3] aborted at entry,
-                      // [4] last-chunk flag, [5] leader polling an event,
-                      // [8..10] leader loop state
+                      // [4] last-chunk flag, [8..10] leader loop state
   TaskDesc* desc;     // [0..1] staged descriptors, [2] the head AOT task's
   uint64_t* times;    // trace: [0] looked-for, [1] ready, [2] operands
                       // staged, [3] last page consumed, [4] body done
@@ -501,28 +510,6 @@ __device__ void issue_gemv_page(const Gemv& g, int p, uint8_t* page,
     bulk_g2s(page + lane * kPagePitch, g.W + (int64_t)wr * g.K + c0, bytes,
              bar, policy);
 }
-__device__ void prefetch_gemv_page(const Gemv& g, int p) {
-  const int lane = threadIdx.x & 31;
-  if (g.b1) {
-    if (lane == 0) {
-      int half, ne;
-      int64_t e0;
-      const uint16_t* src = b1_page(g, p, half, e0, ne);
-      prefetch_l2(src, (uint32_t)ne * 2u);
-    }
-    return;
-  }
-  if (lane >= kPageRows) return;
-  int j, s;
-  page_coords(g, p, j, s);
-  const int c0 = s * kSegCols;
-  bool valid;
-  const int wr = page_wrow(g, j, lane, valid);
-  if (valid)
-    prefetch_l2(g.W + (int64_t)wr * g.K + c0,
-                (uint32_t)min(kSegCols, g.K - c0) * 2u);
-}
-
 // Chunk c of (b, g) covers tokens [t0, t1) of the n = seq_len + 1 positions.
 __device__ __forceinline__ void chunk_range(int c, int n, int C, int& t0,
                                             int& t1) {
@@ -625,73 +612,6 @@ __device__ __forceinline__ bool wait_empty(const KernelParams& P,
   return ok != 0;
 }
 
-// The L2 look-ahead cursor walks the same page sequence as the ring.
-struct Lookahead {
-  int i;        // index into the task list
-  int p, np;    // page within that task, pages of that task (-1: not read)
-  int64_t count;
-  Gemv g;
-  bool gemv;
-};
-
-// Advance the cursor by one page, prefetching it into L2 if asked (and if
-// it is a weight page).  False at the end of the list.
-__device__ bool la_step(const KernelParams& P, const int32_t* list, int n,
-                        Lookahead& la, bool prefetch) {
-  while (la.i < n) {
-    if (la.np < 0) {
-      const TaskDesc t = P.graph.tasks[list[la.i]];
-      la.np = ring_pages_of(P, t, &la.g);
-      la.gemv = is_gemv(t.kind);
-      la.p = 0;
-    }
-    if (la.p < la.np) {
-      if (prefetch && la.gemv && la.g.b1) prefetch_gemv_page(la.g, la.p);
-      ++la.p;
-      ++la.count;
-      return true;
-    }
-    ++la.i;
-    la.np = -1;
-  }
-  return false;
-}
-
-// Bounded wait for a free ring slot (lane 0 spins, the other lanes then
-// observe the phase).  While it waits and the consumers' leader is polling
-// for an event (S.ctrl[5], set around the poll), the HBM stream of this SM
-// would stop; instead lane 0 prefetches the next batch-1 weight pages into
-// L2 (cp.async.bulk.prefetch.L2), up to `pf` pages beyond page `gp`, so the
-// copies after the event hit L2.  In steady streaming the leader is running
-// a task, and nothing is prefetched.
-__device__ bool wait_empty_pf(const KernelParams& P, const Smem& S,
-                              const Ring& ring, uint64_t deadline, int pf,
-                              Lookahead& la, const int32_t* list, int n,
-                              int64_t gp) {
-  const int lane = threadIdx.x & 31;
-  int ok = 1;
-  if (lane == 0) {
-    uint32_t spins = 0;
-    while (!mbar_try_wait(&S.empty[ring.slot], ring.phase ^ 1u)) {
-      if (pf > 0 && S.ctrl[5]) {
-        while (la.count < gp)
-          if (!la_step(P, list, n, la, false)) break;
-        if (la.count < gp + pf && la.i < n) la_step(P, list, n, la, true);
-      }
-      if ((++spins & 1023u) == 0u &&
-          (aborted(P) || globaltimer() > deadline)) {
-        if (!aborted(P)) raise_error(P, MPK_ERR_TIMEOUT);
-        ok = 0;
-        break;
-      }
-    }
-    if (ok && aborted(P)) ok = 0;
-  }
-  ok = __shfl_sync(kFull, ok, 0);
-  if (ok) (void)mbar_try_wait(&S.empty[ring.slot], ring.phase ^ 1u);
-  return ok != 0;
-}
-
 // Producer warp `pid` of kProducerWarps: walks the task list and issues
 // the pages whose global index gp (over the whole list) has
 // gp % kProducerWarps == pid.  The ring position advances by one for every
@@ -707,8 +627,6 @@ __device__ void producer_role(const KernelParams& P, const Smem& S,
 #pragma unroll
   for (int i = 0; i < kMaxRingPages; ++i) issued[i] = 0;
   const uint64_t policy = evict_first_policy();
-  const int pf = pid == 0 ? P.dims.pf_pages : 0;
-  Lookahead la{0, 0, -1, 0, Gemv{}, false};
   Ring ring{0, 0};
   int64_t gp = 0;
   int turn = 0;            // gp % 2
@@ -736,7 +654,7 @@ __device__ void producer_role(const KernelParams& P, const Smem& S,
         }
       }
       if (!mine) continue;
-      if (!wait_empty_pf(P, S, ring, deadline, pf, la, list, n, gp)) {
+      if (!wait_empty(P, S, ring, deadline)) {
         drain_copies(P, S, issued);
         return;
       }
@@ -1175,6 +1093,19 @@ __device__ void gemv_b1(const KernelParams& P, const Smem& S,
   const float4* xb = xa + nch;
   const int np = gemv_pages(g);
   constexpr int kSliceChunks = kSegCols / 8;
+  // Flat pages hold 8 slices; when K / 2048 divides 8, warp w always dots
+  // part w % wpr of x, so that part (64 values a lane) stays in registers
+  // and the loop reads only the weights from shared memory.
+  const bool xreg = g.flat && (kPageRows % g.wpr) == 0;
+  float4 xr[16];
+  if (xreg) {
+    const int xo = (warp % g.wpr) * kSliceChunks + lane;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      xr[2 * k] = xa[xo + 32 * k];
+      xr[2 * k + 1] = xb[xo + 32 * k];
+    }
+  }
   for (int p = 0; p < np; ++p) {
     int half, ne;
     int64_t e0;
@@ -1183,7 +1114,23 @@ __device__ void gemv_b1(const KernelParams& P, const Smem& S,
     if (have) {
       const uint4* pg = reinterpret_cast<const uint4*>(page_ptr(S, ring.slot));
       float* out = S.res + (size_t)half * g.rows * g.wpr;
-      if (g.flat) {
+      if (g.flat && xreg) {
+        // this warp's x slice is the same on every page: in registers
+        const int64_t sl = e0 / kSegCols + warp;
+        if (warp * kSegCols < ne) {
+          const uint4* row = pg + warp * kSliceChunks;
+          float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+          for (int k = 0; k < 8; k += 2) {
+            fma8(row[lane + 32 * k], xr[2 * k], xr[2 * k + 1], a0, a1);
+            fma8(row[lane + 32 * k + 32], xr[2 * k + 2], xr[2 * k + 3], a2,
+                 a3);
+          }
+          const float v = warp_sum(((a0.x + a0.y) + (a1.x + a1.y)) +
+                                   ((a2.x + a2.y) + (a3.x + a3.y)));
+          if (lane == 0) out[sl] = v;
+        }
+      } else if (g.flat) {
         const int64_t sl = e0 / kSegCols + warp;   // slice within the half
         if (warp * kSegCols < ne) {
           const int part = (int)(sl % g.wpr);
@@ -1985,7 +1932,6 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
       int cmd = -1;
       uint32_t spins = 0;
       const int head_dep = (head_id >= 0) ? head->dep : G.end;
-      S.ctrl[5] = 1;   // waiting on an event: the producers may prefetch
       while (!S.ctrl[2]) {
         uint32_t v;
         if (ring_try_pop(jh, js, G.jit_cap, jit_head, v)) {
@@ -2015,7 +1961,6 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
           }
         }
       }
-      S.ctrl[5] = 0;
       *jit_s = (int)jit_head;
       fence_acq_rel_gpu();
       if (G.trace) {
@@ -2122,7 +2067,6 @@ __device__ __forceinline__ bool setup_smem(const KernelParams& P, uint8_t* raw,
     // mpk_reset; read it once per CTA so all threads agree
     S.ctrl[3] = aborted(P) ? 1 : 0;
     S.ctrl[4] = 0;
-    S.ctrl[5] = 0;
     fence_proxy_async_smem();
   }
   __syncthreads();
@@ -2146,10 +2090,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int w = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   if (warp >= kConsumerWarps) {
+    regs_dec<kProducerRegs>();
+    if (warp >= kConsumerWarps + kProducerWarps) return;
     const int a0 = P.graph.aot_off[w], a1 = P.graph.aot_off[w + 1];
     producer_role(P, S, P.graph.aot_list + a0, a1 - a0, deadline,
                   warp - kConsumerWarps);
   } else {
+    regs_inc<kConsumerRegs>();
     worker_consumers(P, S, w, deadline);
   }
 }
@@ -2165,9 +2112,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int task = P.graph.op_tasks[first + blockIdx.x];
   const int warp = threadIdx.x >> 5;
   if (warp >= kConsumerWarps) {
+    regs_dec<kProducerRegs>();
+    if (warp >= kConsumerWarps + kProducerWarps) return;
     producer_role(P, S, P.graph.op_tasks + first + blockIdx.x, 1, deadline,
                   warp - kConsumerWarps);
   } else {
+    regs_inc<kConsumerRegs>();
     Ring ring{0, 0};
     run_task(P, S, P.graph.tasks[task], ring, deadline);
   }

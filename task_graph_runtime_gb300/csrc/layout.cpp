@@ -60,7 +60,7 @@ int lm_head_tiles(const BuiltGraph& bg) {
   return 0;
 }
 
-Dims make_dims(const BuiltGraph& bg, int pf_pages) {
+Dims make_dims(const BuiltGraph& bg) {
   const mpk_model_shape& s = bg.cfg.shape;
   const bool chain = s.chain_ffn > 0;
   Dims D{};
@@ -83,7 +83,6 @@ Dims make_dims(const BuiltGraph& bg, int pf_pages) {
   D.max_ctx = chain ? 1 : s.max_pages_per_seq * s.page_size;
   D.kmax = chain ? std::max(s.hidden, s.chain_ffn)
                  : std::max({s.hidden, s.n_q_heads * s.head_dim, s.ffn});
-  D.pf_pages = pf_pages < 0 ? 0 : pf_pages;
   return D;
 }
 

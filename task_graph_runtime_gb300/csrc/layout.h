@@ -19,8 +19,8 @@ bool smem_layout(const BuiltGraph& bg, int pages_req, int limit,
 // Number of lm_head tiles (the argmax task's fan-in).
 int lm_head_tiles(const BuiltGraph& bg);
 
-// Kernel shape parameters.  `pf_pages`: L2 look-ahead in pages (< 0: none).
-Dims make_dims(const BuiltGraph& bg, int pf_pages);
+// Kernel shape parameters.
+Dims make_dims(const BuiltGraph& bg);
 
 // Activation workspace offsets (A->base left null); returns its size in
 // bytes.  256-byte aligned blocks: one per layer plus one per step.

@@ -172,7 +172,7 @@ extern "C" mpk_status mpk_decode_step_noalloc(
 
   // --- launch parameters pointing into the scratch array
   KernelParams P{};
-  P.dims = make_dims(bg, g->pf_pages);
+  P.dims = make_dims(bg);
   P.sm = sm;
   DevGraph& G = P.graph;
   G.tasks = reinterpret_cast<const TaskDesc*>(base + o_tasks);

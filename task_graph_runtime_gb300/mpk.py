@@ -55,7 +55,6 @@ class TileSizes(ctypes.Structure):
                 ("num_sched_sms", ctypes.c_int),
                 ("sched_warps_per_sm", ctypes.c_int),
                 ("smem_pages", ctypes.c_int),
-                ("l2_prefetch_pages", ctypes.c_int),
                 ("coarse_events", ctypes.c_int)]
 
 
@@ -239,14 +238,14 @@ class Graph:
                  num_sched_sms: int = 0, sched_warps_per_sm: int = 0,
                  smem_pages: int = 0, page_size: int = 16,
                  max_pages_per_seq: int = 1, mma_rows_per_task: int = 0,
-                 l2_prefetch_pages: int = 0, coarse_events: int = 0):
+                 coarse_events: int = 0):
         self.shape = shape
         self.batch = batch
         self.c_shape = model_shape(shape, page_size, max_pages_per_seq)
         self.tiles = TileSizes(num_workers, gemv_rows_per_task,
                                mma_rows_per_task, attn_chunks, num_sched_sms,
                                sched_warps_per_sm, smem_pages,
-                               l2_prefetch_pages, coarse_events)
+                               coarse_events)
         self.handle = mpk_build_tgraph(self.c_shape, self.tiles, batch)
         self._keep = None
 
