@@ -101,18 +101,14 @@ class Op:
 
 def tile_row_cap(batch: int, dual: bool, K: int) -> int:
     """Most output rows of one MatMul tile with reduction length K.  Batch 1:
-    a row's dot product is split into K // 2048 partial sums when K is a
-    multiple of 2048, else into 1 (when 32 KB pages hold 8 or more rows of
-    max(1, 16384 // K)) or 8 // rows partials; the tile's partials fit 2560
-    floats.  Batch 2..7: 64 weight rows; batch >= 8: 128.  A gate/up tile
-    streams two weight rows per output row.  Rounded down to a multiple of
-    8."""
+    32 KB pages hold r = max(1, 16384 // K) whole rows; a row's dot product
+    is one partial sum when r >= 8, else 8 // r partials, and the tile's
+    partials fit 2560 floats.  Batch 2..7: 64 weight rows; batch >= 8: 128.
+    A gate/up tile streams two weight rows per output row.  Rounded down to
+    a multiple of 8."""
     if batch == 1:
-        if K % 2048 == 0:
-            parts = K // 2048
-        else:
-            rpp = max(1, 16384 // K)
-            parts = 1 if rpp >= 8 else 8 // rpp
+        rpp = max(1, 16384 // K)
+        parts = 1 if rpp >= 8 else 8 // rpp
         rows = 2560 // parts
     else:
         rows = 64 if batch < 8 else 128

@@ -119,6 +119,14 @@ bool encode(mpk_graph* g) {
     g->h_aot.insert(g->h_aot.end(), lists[w].begin(), lists[w].end());
   }
   g->h_aot_off[W] = (int32_t)g->h_aot.size();
+  g->h_aot_rec.assign(g->h_aot.size(), AotRec{});
+  for (size_t i = 0; i < g->h_aot.size(); ++i) {
+    AotRec& r = g->h_aot_rec[i];
+    r.desc = g->h_tasks[g->h_aot[i]];
+    r.id = g->h_aot[i];
+    r.dep_count = g->h_events[r.desc.dep].count;
+    r.trig_ev = g->h_events[r.desc.trig];
+  }
   g->h_op_tasks.clear();
   g->h_op_first.clear();
   for (const BOp& o : bg.ops) {
@@ -284,6 +292,8 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
   CK(g->d_events.upload(g->h_events));
   CK(g->d_aot.upload(g->h_aot.empty() ? std::vector<int32_t>{0} : g->h_aot));
   CK(g->d_aot_off.upload(g->h_aot_off));
+  CK(g->d_aot_rec.upload(g->h_aot_rec.empty() ? std::vector<AotRec>(1)
+                                              : g->h_aot_rec));
   CK(g->d_op_tasks.upload(g->h_op_tasks));
   const int nE = (int)g->h_events.size();
   const int S = g->num_sched_sms * g->sched_warps_per_sm;
@@ -332,6 +342,7 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
   G.end = g->bg.end_lin;
   G.aot_list = g->d_aot.p;
   G.aot_off = g->d_aot_off.p;
+  G.aot_rec = g->d_aot_rec.p;
   G.op_tasks = g->d_op_tasks.p;
   G.counters = g->d_counters.p;
   G.merge_cnt = g->d_merge_cnt.p;
@@ -489,9 +500,18 @@ mpk_status mpk_debug_add_event_count(mpk_graph* g, int event, int delta) {
   if (!g || event < 0 || event >= (int)g->h_events.size())
     return MPK_ERR_INVALID_ARG;
   g->h_events[event].count = (uint32_t)((int)g->h_events[event].count + delta);
+  // the AOT records carry copies of their wait and trigger events' counts
+  for (AotRec& r : g->h_aot_rec) {
+    if (r.desc.dep == event) r.dep_count = g->h_events[event].count;
+    if (r.desc.trig == event) r.trig_ev = g->h_events[event];
+  }
   if (g->bound) {
     CK(cudaMemcpy(g->d_events.p + event, &g->h_events[event],
                   sizeof(EventDesc), cudaMemcpyHostToDevice));
+    if (!g->h_aot_rec.empty())
+      CK(cudaMemcpy(g->d_aot_rec.p, g->h_aot_rec.data(),
+                    g->h_aot_rec.size() * sizeof(AotRec),
+                    cudaMemcpyHostToDevice));
   }
   return MPK_OK;
 }

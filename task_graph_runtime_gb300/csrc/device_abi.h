@@ -46,6 +46,19 @@ struct EventDesc {
 };
 static_assert(sizeof(EventDesc) == 16, "event descriptor must stay 16 bytes");
 
+// One entry of a worker's AOT queue with everything its leader needs about
+// the task: the descriptor, the count its dependent event reaches per step,
+// and its triggering event.  Fetched asynchronously while the task before
+// it runs, so dispatch and trigger make no dependent global loads.
+struct AotRec {
+  TaskDesc desc;
+  uint32_t dep_count;
+  int32_t id;          // linear task id
+  uint32_t pad[2];
+  EventDesc trig_ev;
+};
+static_assert(sizeof(AotRec) == 64, "AOT record must stay 64 bytes");
+
 // Multi-producer single-consumer ring in global memory.  Slot value:
 // (ticket << 32) | payload, ticket = position + 1.  Head and tail live on
 // separate 128-byte lines.
@@ -57,13 +70,12 @@ struct RingHdr {
 };
 
 // Weight pages.
-// Batch 1: the rows [i, i + n) of a tile are n * K contiguous elements, so
-// pages are single contiguous bulk copies of at most 32 KB.  When K is a
-// multiple of 2048 ("flat" pages) a page is the next 16384 elements of the
-// tile's row stream and each consumer warp dots one 2048-element slice of
-// one row (K / 2048 partials per row); otherwise a page holds
-// b1_rows_per_page(K) whole rows, each split over b1_warps_per_row(K)
-// warps.
+// Batch 1: the rows [i, i + n) of a tile are n * K contiguous elements, so a
+// page is b1_rows_per_page(K) whole rows (at most 32 KB) in one bulk copy.
+// With 8 or more rows a page, consumer warp w dots rows w, w + 8, ...; with
+// fewer, each row is split over b1_warps_per_row(K) warps into equal column
+// parts, and warp w always takes part w % b1_warps_per_row(K), one partial
+// sum each.
 // Batch > 1: 8 matrix rows x up to 2048 columns, each row one bulk copy,
 // rows kPagePitch bytes apart (16 bytes of skew per row keep ldmatrix reads
 // of 8 rows free of bank conflicts).
@@ -80,13 +92,11 @@ constexpr int kB1Partials = 2560;   // batch-1 row partial sums per tile
 #else
 #define MPK_HD
 #endif
-MPK_HD inline bool b1_flat(int K) { return K % kSegCols == 0; }
 MPK_HD inline int b1_rows_per_page(int K) {
   const int r = (kContigPageBytes / 2) / K;
   return r < 1 ? 1 : r;
 }
 MPK_HD inline int b1_warps_per_row(int K) {
-  if (b1_flat(K)) return K / kSegCols;
   const int r = b1_rows_per_page(K);
   return r >= 8 ? 1 : 8 / r;
 }
@@ -135,6 +145,7 @@ struct DevGraph {
   int root, end;
   const int32_t* aot_list;     // per worker, linear task ids in order
   const int32_t* aot_off;      // [W + 1]
+  const AotRec* aot_rec;       // parallel to aot_list
   const int32_t* op_tasks;     // per operator, linear ids in tile order
   uint32_t* counters;          // [n_events]
   uint32_t* merge_cnt;         // [L][B][Hkv] attention chunk arrivals

@@ -57,9 +57,11 @@ struct mpk_graph {
   std::vector<mpk::TaskDesc> h_tasks;
   std::vector<mpk::EventDesc> h_events;
   std::vector<int32_t> h_aot, h_aot_off, h_op_tasks, h_op_first;
+  std::vector<mpk::AotRec> h_aot_rec;
   DevBuf<mpk::TaskDesc> d_tasks;
   DevBuf<mpk::EventDesc> d_events;
   DevBuf<int32_t> d_aot, d_aot_off, d_op_tasks;
+  DevBuf<mpk::AotRec> d_aot_rec;
   DevBuf<uint32_t> d_counters, d_status, d_merge_cnt;
   DevBuf<mpk::RingHdr> d_jit_hdr, d_sched_hdr;
   DevBuf<uint64_t> d_jit_slots, d_sched_slots;

@@ -163,6 +163,18 @@ __device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
+// 16-byte asynchronous global -> shared copies (one thread's group).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -260,9 +272,11 @@ struct Smem {
   uint64_t* empty;
   volatile int* ctrl; // [0..1] command, [2] bail-out, [3] aborted at entry,
                       // [4] last-chunk flag, [8..10] leader loop state
-  TaskDesc* desc;     // [0..1] staged descriptors, [2] the head AOT task's
+  TaskDesc* desc;     // [0..1] staged descriptors
   uint64_t* times;    // trace: [0] looked-for, [1] ready, [2] operands
                       // staged, [3] last page consumed, [4] body done
+  AotRec* head;       // [2] the head AOT record (by queue position parity)
+  EventDesc* tev;     // [0..1] triggering event of the staged task
   float* scratch;
   int n_pages;
   int page_bytes;
@@ -278,6 +292,8 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const SmemLayout& L) {
   s.ctrl = reinterpret_cast<volatile int*>(base + L.ctrl);
   s.desc = reinterpret_cast<TaskDesc*>(base + L.ctrl + 64);
   s.times = reinterpret_cast<uint64_t*>(base + L.ctrl + 160);
+  s.head = reinterpret_cast<AotRec*>(base + L.ctrl + 224);
+  s.tev = reinterpret_cast<EventDesc*>(base + L.ctrl + 352);
   s.scratch = reinterpret_cast<float*>(base + L.scratch);
   s.n_pages = L.n_pages;
   s.page_bytes = L.page_bytes;
@@ -373,7 +389,7 @@ struct Gemv {
   int row0, rows;       // output rows [row0, row0 + rows)
   int K, N;             // reduction length, output width
   int dual, up_off;
-  int b1, flat, rpp, wpr, pph;
+  int b1, rpp, wpr, pph;
   int ngroups, nsegs;
   const uint16_t* W;
 };
@@ -431,12 +447,9 @@ __device__ Gemv gemv_geom(const KernelParams& P, const TaskDesc& t) {
   g.ngroups = (g.rows + gsize - 1) / gsize;
   g.nsegs = (g.K + kSegCols - 1) / kSegCols;
   g.b1 = D.B == 1 ? 1 : 0;
-  g.flat = b1_flat(g.K) ? 1 : 0;
   g.rpp = b1_rows_per_page(g.K);
   g.wpr = b1_warps_per_row(g.K);
-  constexpr int kFlatElems = kContigPageBytes / 2;
-  g.pph = g.flat ? (int)(((int64_t)g.rows * g.K + kFlatElems - 1) / kFlatElems)
-                 : (g.rows + g.rpp - 1) / g.rpp;
+  g.pph = (g.rows + g.rpp - 1) / g.rpp;
   return g;
 }
 
@@ -452,9 +465,8 @@ __device__ __forceinline__ const uint16_t* b1_page(const Gemv& g, int p,
   half = p / g.pph;
   const int q = p - half * g.pph;
   const int64_t total = (int64_t)g.rows * g.K;
-  e0 = g.flat ? (int64_t)q * (kContigPageBytes / 2)
-              : (int64_t)q * g.rpp * g.K;
-  const int64_t span = g.flat ? (kContigPageBytes / 2) : (int64_t)g.rpp * g.K;
+  e0 = (int64_t)q * g.rpp * g.K;
+  const int64_t span = (int64_t)g.rpp * g.K;
   ne = (int)min(span, total - e0);
   return g.W + ((int64_t)(half ? g.up_off : 0) + g.row0) * g.K + e0;
 }
@@ -636,9 +648,7 @@ __device__ void producer_role(const KernelParams& P, const Smem& S,
     const int np = ring_pages_of(P, t, &g);
     // batch-1 weight pages: source pointer and length advance linearly
     const bool lin = np > 0 && is_gemv(t.kind) && g.b1;
-    const int64_t span = lin ? (g.flat ? (int64_t)(kContigPageBytes / 2)
-                                       : (int64_t)g.rpp * g.K)
-                             : 0;
+    const int64_t span = lin ? (int64_t)g.rpp * g.K : 0;
     const int64_t total = (int64_t)g.rows * g.K;
     int64_t e0 = 0;
     int half = 0;
@@ -1077,87 +1087,107 @@ __device__ __forceinline__ float row_dot(const uint4* row, const float4* xa,
                   ((a2.x + a2.y) + (a3.x + a3.y)));
 }
 
-// Batch 1.  Flat pages: warp w dots slice w of the page (2048 elements of
-// one row).  Whole-row pages: with 8 or more rows per page warp w takes
-// rows w, w + 8, ...; with fewer, each row is split over wpr warps into
-// column ranges of equal length (multiples of 8), one partial each.
+// Dot of this lane's NCK chunks row[lane + 32 k] with the x chunks held in
+// registers (two float4 halves per chunk), summed over the warp.
+template <int NCK>
+__device__ __forceinline__ float row_dot_xreg(const uint4* row,
+                                              const float4 (&xr)[16]) {
+  const int lane = threadIdx.x & 31;
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+  uint4 w[NCK > 0 ? NCK : 1];
+#pragma unroll
+  for (int k = 0; k < NCK; ++k) w[k] = row[lane + 32 * k];
+#pragma unroll
+  for (int k = 0; k < NCK; ++k) {
+    if (k & 1) fma8(w[k], xr[2 * k], xr[2 * k + 1], a2, a3);
+    else fma8(w[k], xr[2 * k], xr[2 * k + 1], a0, a1);
+  }
+  return warp_sum(((a0.x + a0.y) + (a1.x + a1.y)) +
+                  ((a2.x + a2.y) + (a3.x + a3.y)));
+}
+
+// One batch-1 page of whole rows [i0, i0 + n).  With NCK > 0 this warp's x
+// part (NCK 32-chunk strides) is in registers; NCK == 0 reads x from shared
+// memory.
+template <int NCK>
+__device__ __forceinline__ void b1_page_rows(const uint4* pg, float* out,
+                                             const Gemv& g, int i0, int n,
+                                             bool multi, int part, int nch,
+                                             int c0, int c1, const float4* xa,
+                                             const float4* xb,
+                                             const float4 (&xr)[16]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (multi) {
+    for (int r = warp; r < n; r += kConsumerWarps) {
+      const uint4* row = pg + (size_t)r * nch;
+      const float v = NCK > 0 ? row_dot_xreg<NCK>(row, xr)
+                              : row_dot(row, xa, xb, 0, nch);
+      if (lane == 0) out[i0 + r] = v;
+    }
+  } else {
+    const int r = warp / g.wpr;
+    if (r < n) {
+      const uint4* row = pg + (size_t)r * nch;
+      const float v = NCK > 0 ? row_dot_xreg<NCK>(row + c0, xr)
+                              : row_dot(row, xa, xb, c0, c1);
+      if (lane == 0) out[(i0 + r) * g.wpr + part] = v;
+    }
+  }
+}
+
+// Batch 1.  Pages hold whole rows.  With 8 or more rows per page warp w
+// takes rows w, w + 8, ...; with fewer, each row is split over wpr warps into
+// column parts of equal length and warp w always takes part w % wpr.  When
+// a warp's part is 1, 2, 4, 6 or 8 strides of 32 chunks, its x values stay
+// in registers for the whole tile and the loop reads only the weights from
+// shared memory.
+template <int NCK>
+__device__ void gemv_b1_loop(const KernelParams& P, const Smem& S,
+                             const Gemv& g, Ring& ring, uint64_t deadline,
+                             bool multi, int part, int nch, int c0, int c1) {
+  const int lane = threadIdx.x & 31;
+  const float4* xa = reinterpret_cast<const float4*>(S.xs);
+  const float4* xb = xa + nch;
+  float4 xr[16];
+#pragma unroll
+  for (int k = 0; k < NCK; ++k) {
+    xr[2 * k] = xa[c0 + lane + 32 * k];
+    xr[2 * k + 1] = xb[c0 + lane + 32 * k];
+  }
+  const int halves = g.dual ? 2 : 1;
+  for (int half = 0; half < halves; ++half) {
+    float* out = S.res + (size_t)half * g.rows * g.wpr;
+    for (int i0 = 0; i0 < g.rows; i0 += g.rpp) {
+      const int n = min(g.rpp, g.rows - i0);
+      const bool have = wait_full(P, S, ring, deadline);
+      if (have)
+        b1_page_rows<NCK>(
+            reinterpret_cast<const uint4*>(page_ptr(S, ring.slot)), out, g,
+            i0, n, multi, part, nch, c0, c1, xa, xb, xr);
+      release_page(S, ring, have);
+    }
+  }
+}
+
 __device__ void gemv_b1(const KernelParams& P, const Smem& S,
                         const TaskDesc& t, const Gemv& g, Ring& ring,
                         uint64_t deadline) {
   stage_x_b1(P, S, t, g);
   stamp(P, S, 2);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5;
   const int nch = g.K >> 3;
-  const int cpw = (nch + g.wpr - 1) / g.wpr;
-  const float4* xa = reinterpret_cast<const float4*>(S.xs);
-  const float4* xb = xa + nch;
-  const int np = gemv_pages(g);
-  constexpr int kSliceChunks = kSegCols / 8;
-  // Flat pages hold 8 slices; when K / 2048 divides 8, warp w always dots
-  // part w % wpr of x, so that part (64 values a lane) stays in registers
-  // and the loop reads only the weights from shared memory.
-  const bool xreg = g.flat && (kPageRows % g.wpr) == 0;
-  float4 xr[16];
-  if (xreg) {
-    const int xo = (warp % g.wpr) * kSliceChunks + lane;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      xr[2 * k] = xa[xo + 32 * k];
-      xr[2 * k + 1] = xb[xo + 32 * k];
-    }
-  }
-  for (int p = 0; p < np; ++p) {
-    int half, ne;
-    int64_t e0;
-    b1_page(g, p, half, e0, ne);
-    const bool have = wait_full(P, S, ring, deadline);
-    if (have) {
-      const uint4* pg = reinterpret_cast<const uint4*>(page_ptr(S, ring.slot));
-      float* out = S.res + (size_t)half * g.rows * g.wpr;
-      if (g.flat && xreg) {
-        // this warp's x slice is the same on every page: in registers
-        const int64_t sl = e0 / kSegCols + warp;
-        if (warp * kSegCols < ne) {
-          const uint4* row = pg + warp * kSliceChunks;
-          float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-#pragma unroll
-          for (int k = 0; k < 8; k += 2) {
-            fma8(row[lane + 32 * k], xr[2 * k], xr[2 * k + 1], a0, a1);
-            fma8(row[lane + 32 * k + 32], xr[2 * k + 2], xr[2 * k + 3], a2,
-                 a3);
-          }
-          const float v = warp_sum(((a0.x + a0.y) + (a1.x + a1.y)) +
-                                   ((a2.x + a2.y) + (a3.x + a3.y)));
-          if (lane == 0) out[sl] = v;
-        }
-      } else if (g.flat) {
-        const int64_t sl = e0 / kSegCols + warp;   // slice within the half
-        if (warp * kSegCols < ne) {
-          const int part = (int)(sl % g.wpr);
-          const int xo = part * kSliceChunks;
-          const float v = row_dot(pg + warp * kSliceChunks, xa + xo, xb + xo,
-                                  0, kSliceChunks);
-          if (lane == 0) out[sl] = v;
-        }
-      } else {
-        const int i0 = (int)(e0 / g.K), n = ne / g.K;
-        if (g.rpp >= kPageRows) {
-          for (int r = warp; r < n; r += kConsumerWarps) {
-            const float v = row_dot(pg + (size_t)r * nch, xa, xb, 0, nch);
-            if (lane == 0) out[i0 + r] = v;
-          }
-        } else {
-          const int r = warp / g.wpr, part = warp - r * g.wpr;
-          if (r < n) {
-            const int c0 = part * cpw;
-            const float v =
-                row_dot(pg + (size_t)r * nch, xa, xb, c0, min(nch, c0 + cpw));
-            if (lane == 0) out[(i0 + r) * g.wpr + part] = v;
-          }
-        }
-      }
-    }
-    release_page(S, ring, have);
+  const bool multi = g.rpp >= kPageRows;
+  const int part = multi ? 0 : warp % g.wpr;
+  const int cpw = multi ? nch : (nch + g.wpr - 1) / g.wpr;
+  const int c0 = part * cpw, c1 = min(nch, c0 + cpw);
+  const bool even = (cpw & 31) == 0 && (multi || nch % g.wpr == 0);
+  switch (even ? cpw >> 5 : 0) {
+    case 8: gemv_b1_loop<8>(P, S, g, ring, deadline, multi, part, nch, c0, c1); break;
+    case 6: gemv_b1_loop<6>(P, S, g, ring, deadline, multi, part, nch, c0, c1); break;
+    case 4: gemv_b1_loop<4>(P, S, g, ring, deadline, multi, part, nch, c0, c1); break;
+    case 2: gemv_b1_loop<2>(P, S, g, ring, deadline, multi, part, nch, c0, c1); break;
+    case 1: gemv_b1_loop<1>(P, S, g, ring, deadline, multi, part, nch, c0, c1); break;
+    default: gemv_b1_loop<0>(P, S, g, ring, deadline, multi, part, nch, c0, c1); break;
   }
   consumer_sync();
   stamp(P, S, 3);
@@ -1853,40 +1883,46 @@ __device__ __forceinline__ bool ring_try_pop(RingHdr* hdr, uint64_t* slots,
   return true;
 }
 
-// Fire `e` (one trigger).  The activating trigger pushes the event to its
-// scheduler warp when it has JIT tasks, and runs its empty tasks inline
-// (they only trigger their own event).
-__device__ void trigger(const KernelParams& P, int e, uint64_t deadline) {
+// Fire `e` (one trigger), whose descriptor `ed0` the caller holds.  The
+// activating trigger pushes the event to its scheduler warp when it has JIT
+// tasks, and runs its empty tasks inline (they only trigger their own
+// event, whose descriptor is read from the graph).
+__device__ void trigger(const KernelParams& P, int e, const EventDesc& ed0,
+                        uint64_t deadline) {
   const DevGraph& G = P.graph;
   const uint32_t epoch = P.step.epoch;
   int stack[16];
   int sp = 0;
-  stack[sp++] = e;
-  while (sp > 0) {
-    const int ev = stack[--sp];
-    const EventDesc ed = G.events[ev];
+  int ev = e;
+  EventDesc ed = ed0;
+  while (true) {
     if (!(ed.flags & (EV_HAS_JIT | EV_HAS_INLINE))) {
       red_release_add(G.counters + ev, 1u);
-      continue;
-    }
-    const uint32_t old = atom_acq_rel_add(G.counters + ev, 1u);
-    if (old + 1u != epoch * ed.count) continue;
-    if (ed.flags & EV_HAS_JIT) {
-      const int s = ev % G.S;
-      if (!ring_push(P, G.sched_hdr + s, G.sched_slots + (size_t)s * G.sched_cap,
-                     G.sched_cap, (uint32_t)ev, deadline))
-        return;
-    }
-    if (ed.flags & EV_HAS_INLINE) {
-      const int n_in = (int)(ed.flags >> kEvInlineShift);
-      for (int t = ed.last - n_in + 1; t <= ed.last; ++t) {
-        if (sp >= 16) {
-          raise_error(P, MPK_ERR_QUEUE_OVERFLOW);
-          return;
+    } else {
+      const uint32_t old = atom_acq_rel_add(G.counters + ev, 1u);
+      if (old + 1u == epoch * ed.count) {
+        if (ed.flags & EV_HAS_JIT) {
+          const int s = ev % G.S;
+          if (!ring_push(P, G.sched_hdr + s,
+                         G.sched_slots + (size_t)s * G.sched_cap, G.sched_cap,
+                         (uint32_t)ev, deadline))
+            return;
         }
-        stack[sp++] = G.tasks[t].trig;
+        if (ed.flags & EV_HAS_INLINE) {
+          const int n_in = (int)(ed.flags >> kEvInlineShift);
+          for (int t = ed.last - n_in + 1; t <= ed.last; ++t) {
+            if (sp >= 16) {
+              raise_error(P, MPK_ERR_QUEUE_OVERFLOW);
+              return;
+            }
+            stack[sp++] = G.tasks[t].trig;
+          }
+        }
       }
     }
+    if (sp == 0) return;
+    ev = stack[--sp];
+    ed = G.events[ev];
   }
 }
 
@@ -1896,58 +1932,78 @@ __device__ __forceinline__ bool event_done(const KernelParams& P, int e) {
 }
 
 // ------------------------------------------------------------ roles
+// Asynchronous fetch of one AOT record into shared memory (thread 0).
+__device__ __forceinline__ void fetch_rec(const AotRec* src, AotRec* dst) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) cp_async16(d + i, s + i);
+  cp_async_commit();
+}
+
 // Leader-only loop state lives in shared memory (S.ctrl[8..10]) rather than
-// in registers that every thread would carry across the task bodies.
+// in registers that every thread would carry across the task bodies.  The
+// head AOT record is fetched asynchronously as soon as the task before it
+// is dispatched, so the poll, the dispatch and the trigger read nothing
+// from global memory but the event counter.
 __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
                                  uint64_t deadline) {
   const DevGraph& G = P.graph;
   const int tid = threadIdx.x;
-  volatile int* ai_s = S.ctrl + 8;        // next AOT list position
-  volatile int* head_s = S.ctrl + 9;      // its task id, -1 past the end
+  volatile int* ai_s = S.ctrl + 8;        // queue position of the head record
+  volatile int* a1_s = S.ctrl + 9;        // end of this worker's AOT queue
   volatile int* jit_s = S.ctrl + 10;      // JIT ring head
-  // The head AOT task's descriptor is prefetched into shared memory as soon
-  // as the task before it is dispatched, before its event is polled.
-  TaskDesc* head = &S.desc[2];
   if (tid == 0) {
     const int a0 = G.aot_off[w], a1 = G.aot_off[w + 1];
     *jit_s = (int)ld_relaxed(&G.jit_hdr[w].head);
     *ai_s = a0;
-    *head_s = -1;
-    if (a0 < a1) {
-      *head_s = G.aot_list[a0];
-      *head = G.tasks[*head_s];
-    }
+    *a1_s = a1;
+    if (a0 < a1) fetch_rec(G.aot_rec + a0, &S.head[a0 & 1]);
   }
   Ring ring{0, 0};
   int iter = 0;
   while (true) {
+    const int slot = iter & 1;
     if (tid == 0) {
       if (G.trace) S.times[0] = globaltimer();
-      int head_id = *head_s;
-      // warm L2 with the head task's weight-side prologue operand
-      if (head_id >= 0) prefetch_gain(P, *head);
+      const int ai = *ai_s;
+      const bool have_head = ai < *a1_s;
+      cp_async_wait_all();
+      const AotRec* hr = &S.head[ai & 1];
+      int dep;
+      uint32_t target;
+      if (have_head) {
+        prefetch_gain(P, hr->desc);   // warm L2 with the prologue's gain
+        dep = hr->desc.dep;
+        target = P.step.epoch * hr->dep_count;
+      } else {
+        dep = G.end;
+        target = P.step.epoch * G.events[G.end].count;
+      }
       RingHdr* jh = G.jit_hdr + w;
       uint64_t* js = G.jit_slots + (size_t)w * G.jit_cap;
       uint32_t jit_head = (uint32_t)*jit_s;
       int cmd = -1;
       uint32_t spins = 0;
-      const int head_dep = (head_id >= 0) ? head->dep : G.end;
       while (!S.ctrl[2]) {
         uint32_t v;
         if (ring_try_pop(jh, js, G.jit_cap, jit_head, v)) {
           cmd = (int)v;
-          S.desc[iter & 1] = G.tasks[cmd];
+          S.desc[slot] = G.tasks[cmd];
+          S.tev[slot] = G.events[S.desc[slot].trig];
           break;
         }
-        if (event_done(P, head_dep)) {
-          cmd = head_id;   // -1 when the end event fired
-          if (head_id >= 0) {
-            S.desc[iter & 1] = *head;
-            const int ai = *ai_s + 1;
-            *ai_s = ai;
-            head_id = (ai < G.aot_off[w + 1]) ? G.aot_list[ai] : -1;
-            *head_s = head_id;
-            if (head_id >= 0) *head = G.tasks[head_id];
+        // the acquire orders this CTA's later reads after the producers'
+        // releasing triggers (passed on to the other threads by the barrier
+        // below)
+        if ((int32_t)(ld_acquire(G.counters + dep) - target) >= 0) {
+          if (have_head) {
+            cmd = hr->id;
+            S.desc[slot] = hr->desc;
+            S.tev[slot] = hr->trig_ev;
+            *ai_s = ai + 1;
+            if (ai + 1 < *a1_s)
+              fetch_rec(G.aot_rec + ai + 1, &S.head[(ai + 1) & 1]);
           }
           break;
         }
@@ -1962,16 +2018,14 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
         }
       }
       *jit_s = (int)jit_head;
-      fence_acq_rel_gpu();
       if (G.trace) {
         S.times[1] = globaltimer();
         S.times[2] = S.times[3] = 0;
       }
-      S.ctrl[iter & 1] = cmd;
+      S.ctrl[slot] = cmd;
     }
     consumer_sync();
-    const int cmd = S.ctrl[iter & 1];
-    const int slot = iter & 1;
+    const int cmd = S.ctrl[slot];
     ++iter;
     if (cmd < 0) break;
     run_task(P, S, S.desc[slot], ring, deadline);
@@ -1983,7 +2037,7 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
       // the red.release / atom.acq_rel of the trigger is cumulative: it
       // orders every write of the CTA that the barrier above ordered before
       // this thread
-      trigger(P, S.desc[slot].trig, deadline);
+      trigger(P, S.desc[slot].trig, S.tev[slot], deadline);
       if (G.trace) {
         // (task | worker << 32), looked-for, ready, staged, pages done,
         // body done, triggered
@@ -2002,6 +2056,7 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
       }
     }
   }
+  if (tid == 0) cp_async_wait_all();
 }
 
 __device__ void scheduler_role(const KernelParams& P, int s,

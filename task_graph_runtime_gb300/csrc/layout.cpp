@@ -42,7 +42,7 @@ bool smem_layout(const BuiltGraph& bg, int pages_req, int limit,
     L.bars = off;
     off = round_up(off + 16 * pages, 128);
     L.ctrl = off;
-    off += 256;   // control words, 3 staged descriptors, 2 trace times
+    off += 384;   // control words, staged descriptors and records, times
     L.scratch = off;
     off += 512;
     L.total = off;

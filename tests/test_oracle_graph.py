@@ -235,7 +235,9 @@ def test_row_tiles_cover_rows():
 def test_tile_caps_by_batch():
     assert tgraph.tile_row_cap(1, False, 4096) == 1280     # 4 rows/page, 2 warps/row
     assert tgraph.tile_row_cap(1, True, 4096) == 640
-    assert tgraph.tile_row_cap(1, False, 12288) == 424     # 6 slices/row
+    assert tgraph.tile_row_cap(1, False, 12288) == 320     # 1 row/page, 8 parts
+    assert tgraph.tile_row_cap(1, False, 8192) == 640      # 2 rows/page, 4 parts
+    assert tgraph.tile_row_cap(1, False, 6144) == 640      # 2 rows/page, 4 parts
     assert tgraph.tile_row_cap(1, False, 688) == 2560      # 23 rows/page
     assert tgraph.tile_row_cap(1, False, 2048) == 2560     # 8 rows/page
     assert tgraph.tile_row_cap(1, False, 256) == 2560
