@@ -277,6 +277,8 @@ struct Smem {
                       // staged, [3] last page consumed, [4] body done
   AotRec* head;       // [2] the head AOT record (by queue position parity)
   EventDesc* tev;     // [0..1] triggering event of the staged task
+  int2* meta;         // [ring slot] (position, new token's KV page) of the
+                      // AOT attention task whose K page is in that slot
   float* scratch;
   int n_pages;
   int page_bytes;
@@ -294,6 +296,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const SmemLayout& L) {
   s.times = reinterpret_cast<uint64_t*>(base + L.ctrl + 160);
   s.head = reinterpret_cast<AotRec*>(base + L.ctrl + 224);
   s.tev = reinterpret_cast<EventDesc*>(base + L.ctrl + 352);
+  s.meta = reinterpret_cast<int2*>(base + L.ctrl + 384);
   s.scratch = reinterpret_cast<float*>(base + L.scratch);
   s.n_pages = L.n_pages;
   s.page_bytes = L.page_bytes;
@@ -535,7 +538,7 @@ __device__ __forceinline__ void chunk_range(int c, int n, int C, int& t0,
 // Lane 0 only.
 __device__ void issue_attn_page(const KernelParams& P, const TaskDesc& t,
                                 int which, uint8_t* page, uint64_t* bar,
-                                uint64_t policy) {
+                                uint64_t policy, int2* meta) {
   const Dims& D = P.dims;
   const int b = t.b, pos = __ldcg(P.step.seq_lens + b);
   const int n = pos + 1;
@@ -546,6 +549,12 @@ __device__ void issue_attn_page(const KernelParams& P, const TaskDesc& t,
   const int P_ = D.page_size, d = D.d;
   const uint32_t row_bytes = (uint32_t)d * 2u;
   const int32_t* pt = P.step.page_table + (int64_t)b * D.max_pages;
+  if (meta) {
+    // the consumers read these after the K page's arrival (the arrive
+    // below releases them)
+    const int pidx = ok ? pos / P_ : D.max_pages;
+    *meta = make_int2(pos, pidx < D.max_pages ? __ldg(pt + pidx) : -1);
+  }
   const int64_t head_elems = (int64_t)P_ * d;
   const int64_t layer_elems =
       (int64_t)t.layer * P.step.num_pages * D.Hkv * head_elems;
@@ -681,7 +690,8 @@ __device__ void producer_role(const KernelParams& P, const Smem& S,
       } else if (is_gemv(t.kind)) {
         issue_gemv_page(g, p, page, bar, policy);
       } else if (lane == 0) {
-        issue_attn_page(P, t, p, page, bar, policy);   // p 0: K, 1: V
+        issue_attn_page(P, t, p, page, bar, policy,   // p 0: K, 1: V
+                        p == 0 ? &S.meta[ring.slot] : nullptr);
       }
       __syncwarp();
       issued[ring.slot] = 1u | (ring.phase << 1);
@@ -1438,8 +1448,8 @@ __device__ __forceinline__ void load_row_cg(const uint16_t* p, int DLc,
 
 // Row `tok` of the K (or V) chunk, this lane's DL values: from the ring
 // page (AOT) or the paged cache (JIT); zero past the chunk.
-template <int DL>
-__device__ __forceinline__ void attn_row(const KernelParams& P, bool pre,
+template <int DL, bool PRE>
+__device__ __forceinline__ void attn_row(const KernelParams& P,
                                          const uint8_t* page,
                                          const uint16_t* pool, int tok,
                                          int t0, int t1, int64_t layer_elems,
@@ -1449,20 +1459,60 @@ __device__ __forceinline__ void attn_row(const KernelParams& P, bool pre,
 #pragma unroll
   for (int e = 0; e < DL; ++e) out[e] = 0.f;
   if (tok >= t1) return;
-  if (pre) {
+  if constexpr (PRE) {
     load_row(reinterpret_cast<const uint16_t*>(page) + (size_t)(tok - t0) * d +
                  lane * DL,
              DL, out);
-    return;
+  } else {
+    const Dims& D = P.dims;
+    const int page_id = __ldg(pt + tok / D.page_size);
+    if (page_id >= 0 && page_id < P.step.num_pages) {
+      load_row_cg(pool + layer_elems + (int64_t)page_id * D.Hkv * head_elems +
+                      (int64_t)(tok % D.page_size) * d + lane * DL,
+                  DL, out);
+    } else if (lane == 0) {
+      raise_error(P, MPK_ERR_KV_PAGE);
+    }
   }
-  const Dims& D = P.dims;
-  const int page_id = __ldg(pt + tok / D.page_size);
-  if (page_id >= 0 && page_id < P.step.num_pages) {
-    load_row_cg(pool + layer_elems + (int64_t)page_id * D.Hkv * head_elems +
-                    (int64_t)(tok % D.page_size) * d + lane * DL,
-                DL, out);
-  } else if (lane == 0) {
-    raise_error(P, MPK_ERR_KV_PAGE);
+}
+
+// Merge the 8 warps' (m, l, acc) records of wbuf ([warp][GRP][2 + d]) per
+// head: the factors exp(m_w - M) and the sum L are formed once per head
+// (S.scratch), then thread i of the head's d outputs sums its column.
+// Returns through `emit(h, i, A, L)` for the outputs this thread owns.
+template <int GRP, int d, typename Emit>
+__device__ __forceinline__ void merge_warps(const Smem& S, const float* wbuf,
+                                            Emit emit) {
+  constexpr int rec = 2 + d;
+  const int tid = threadIdx.x;
+  float* fac = S.scratch;                       // [GRP][8]
+  float* lsum = S.scratch + GRP * kConsumerWarps;   // [GRP]
+  if (tid < GRP) {
+    const int h = tid;
+    float M = -INFINITY;
+    for (int w = 0; w < kConsumerWarps; ++w)
+      M = fmaxf(M, wbuf[(w * GRP + h) * rec]);
+    float Ls = 0.f;
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float* r = wbuf + (w * GRP + h) * rec;
+      const float sc =
+          (M == -INFINITY || r[0] == -INFINITY) ? 0.f : expf(r[0] - M);
+      fac[h * kConsumerWarps + w] = sc;
+      Ls = fmaf(r[1], sc, Ls);
+    }
+    lsum[h] = Ls;
+    // the merged maximum replaces warp 0's for the caller
+    S.scratch[GRP * (kConsumerWarps + 1) + h] = M;
+  }
+  consumer_sync();
+  for (int o = tid; o < GRP * d; o += kConsumers) {
+    const int h = o / d, i = o - h * d;
+    float A = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w)
+      A = fmaf(wbuf[(w * GRP + h) * rec + 2 + i], fac[h * kConsumerWarps + w],
+               A);
+    emit(h, i, A, lsum[h], S.scratch[GRP * (kConsumerWarps + 1) + h]);
   }
 }
 
@@ -1474,46 +1524,50 @@ __device__ __forceinline__ void attn_row(const KernelParams& P, bool pre,
 // block scores token j/GRP against head j%GRP).  The warps merge into one
 // (m, l, acc) partial per head; the last chunk of (b, g) to finish merges
 // the C partials (log-sum-exp) into the bf16 attention output.  AOT tasks
-// read their cached tokens from two ring pages the producer filled ahead of
-// time; JIT tasks read the paged cache directly.
-template <int DL, int GRP>
+// (PRE) read their cached tokens from two ring pages the producer filled
+// ahead of time, and the position from the producer's note beside the K
+// page; JIT tasks read the paged cache directly.
+template <int DL, int GRP, bool PRE>
 __device__ void attn_body(const KernelParams& P, const Smem& S,
                           const TaskDesc& t, Ring& ring, uint64_t deadline) {
-  constexpr int d = DL * 32, TB = 32 / GRP;
+  constexpr int d = DL * 32, TB = 32 / GRP, rec = 2 + d;
   const Dims& D = P.dims;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = t.b, g = t.g, l = t.layer, C = D.C;
-  const bool pre = t.launch == MPK_LAUNCH_AOT;
-  const int pos = __ldcg(P.step.seq_lens + b);
-  const int n = pos + 1;
   float* qf = reinterpret_cast<float*>(S.xs);       // [GRP][d]
-  float* knew = qf + GRP * d;                        // [d]
-  float* vnew = knew + d;                            // [d]
-  float* wbuf = vnew + d;                            // [8][GRP][2 + d]
+  float* wbuf = qf + GRP * d;                        // [8][GRP][2 + d]
   bool have_k = true, have_v = true;
   uint8_t *kpage = nullptr, *vpage = nullptr;
   Ring kr = ring;
-  if (pre) {
+  int pos, page_new = -1;
+  if constexpr (PRE) {
     have_k = wait_full(P, S, ring, deadline);
     kpage = page_ptr(S, ring.slot);
+    const int2 m = S.meta[ring.slot];
+    pos = have_k ? m.x : -1;
+    page_new = m.y;
     ring.advance(S.n_pages);
     have_v = wait_full(P, S, ring, deadline);
     vpage = page_ptr(S, ring.slot);
     ring.advance(S.n_pages);
+  } else {
+    pos = __ldcg(P.step.seq_lens + b);
   }
+  const int n = pos + 1;
   int t0 = 0, t1 = 0;
-  int page_new = -1;
   bool ok = pos >= 0 && n <= D.max_ctx;
   if (ok) {
     chunk_range(t.c, n, C, t0, t1);
-    if (pre) t1 = min(t1, t0 + kAttnMaxTokens);
-    const int pidx = pos / D.page_size;
-    if (pidx < D.max_pages)
-      page_new = __ldg(P.step.page_table + (int64_t)b * D.max_pages + pidx);
+    if (PRE) t1 = min(t1, t0 + kAttnMaxTokens);
+    if (!PRE) {
+      const int pidx = pos / D.page_size;
+      if (pidx < D.max_pages)
+        page_new = __ldg(P.step.page_table + (int64_t)b * D.max_pages + pidx);
+    }
     ok = page_new >= 0 && page_new < P.step.num_pages;
   }
   if (!ok) {
-    if (tid == 0) raise_error(P, MPK_ERR_KV_PAGE);
+    if (tid == 0 && have_k) raise_error(P, MPK_ERR_KV_PAGE);
     t0 = t1 = 0;
   }
   const bool has_new = ok && t1 == n && t1 > t0;
@@ -1542,12 +1596,12 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
       }
       float x[DL];
       rope_head<DL>(P, src, nw, cs, hh <= GRP, x);
-      float* dst = hh < GRP ? qf + hh * d : (hh == GRP ? knew : vnew);
+      if (hh < GRP) {
 #pragma unroll
-      for (int e = 0; e < DL; ++e) dst[lane * DL + e] = x[e];
-      if (hh >= GRP) {
+        for (int e = 0; e < DL; ++e) qf[hh * d + lane * DL + e] = x[e];
+      } else {
         uint16_t* cache = (hh == GRP ? P.step.k_pool : P.step.v_pool) + slot;
-        uint16_t* pg = pre ? reinterpret_cast<uint16_t*>(
+        uint16_t* pg = PRE ? reinterpret_cast<uint16_t*>(
                                  (hh == GRP ? kpage : vpage)) +
                                  (size_t)(pos - t0) * d
                            : nullptr;
@@ -1555,11 +1609,11 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
         for (int e = 0; e < DL; ++e) {
           const uint16_t u = f2bf(x[e]);
           cache[lane * DL + e] = u;
-          if (pg) pg[lane * DL + e] = u;
+          if (PRE) pg[lane * DL + e] = u;
         }
       }
     }
-    if (!pre) __threadfence();   // the new K/V row is read back below
+    if (!PRE) __threadfence();   // the new K/V row is read back below
     consumer_sync();
   }
   stamp(P, S, 2);
@@ -1589,8 +1643,8 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
     for (int tb = 0; tb < TB; ++tb) {
       const int tok = t0 + blk * TB + tb;
       float kf[DL];
-      attn_row(P, pre, kpage, P.step.k_pool, tok, t0, t1, layer_elems,
-               head_elems, pt, kf);
+      attn_row<DL, PRE>(P, kpage, P.step.k_pool, tok, t0, t1, layer_elems,
+                        head_elems, pt, kf);
 #pragma unroll
       for (int h = 0; h < GRP; ++h) {
         float s = 0.f;
@@ -1625,8 +1679,8 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
     for (int tb = 0; tb < TB; ++tb) {
       const int tok = t0 + blk * TB + tb;
       float vf[DL];
-      attn_row(P, pre, vpage, P.step.v_pool, tok, t0, t1, layer_elems,
-               head_elems, pt, vf);
+      attn_row<DL, PRE>(P, vpage, P.step.v_pool, tok, t0, t1, layer_elems,
+                        head_elems, pt, vf);
 #pragma unroll
       for (int h = 0; h < GRP; ++h) {
         const float pth = __shfl_sync(kFull, p, tb * GRP + h);
@@ -1636,7 +1690,7 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
     }
   }
   stamp(P, S, 3);
-  if (pre) {
+  if constexpr (PRE) {
     // the pages were written through the generic proxy (new token): order
     // that before the producer's next bulk copy into them
     fence_proxy_async_smem();
@@ -1644,7 +1698,6 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
     release_page(S, kr, have_v);
   }
   // ---- merge the 8 warps into this chunk's partial
-  constexpr int rec = 2 + d;
 #pragma unroll
   for (int h = 0; h < GRP; ++h) {
     float* r = wbuf + (warp * GRP + h) * rec;
@@ -1661,28 +1714,13 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
   float* part = lt<float>(P, l, P.act.o_opart) +
                 (((int64_t)(b * D.Hkv + g) * C) * GRP) * rec;
   float* mine = part + (int64_t)t.c * GRP * rec;
-  for (int o = tid; o < GRP * d; o += kConsumers) {
-    const int h = o / d, i = o - h * d;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w)
-      M = fmaxf(M, wbuf[(w * GRP + h) * rec]);
-    float Ls = 0.f, A = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float* r = wbuf + (w * GRP + h) * rec;
-        const float sc = (r[0] == -INFINITY) ? 0.f : expf(r[0] - M);
-        Ls = fmaf(r[1], sc, Ls);
-        A = fmaf(r[2 + i], sc, A);
-      }
-    }
+  merge_warps<GRP, d>(S, wbuf, [=](int h, int i, float A, float Ls, float M) {
     mine[h * rec + 2 + i] = A;
     if (i == 0) {
       mine[h * rec] = M;
       mine[h * rec + 1] = Ls;
     }
-  }
+  });
   __threadfence();
   consumer_sync();
   // ---- the last chunk of (b, g) to finish merges all C partials
@@ -1706,7 +1744,7 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
 #pragma unroll
       for (int e = 0; e < DL; ++e) Aw[h][e] = 0.f;
     }
-#pragma unroll 2
+#pragma unroll 1
     for (int c = warp; c < C; c += kConsumerWarps) {
       const float* rc = part + (int64_t)c * GRP * rec;
       float mc[GRP], lc[GRP], ac[GRP][DL];
@@ -1730,7 +1768,7 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
         Mw[h] = Mn;
       }
     }
-    consumer_sync();   // wbuf is reused
+    consumer_sync();   // wbuf and the scratch factors are reused
 #pragma unroll
     for (int h = 0; h < GRP; ++h) {
       float* r = wbuf + (warp * GRP + h) * rec;
@@ -1745,39 +1783,36 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
   }
   uint16_t* out = lt(P, l, P.act.o_attn) + (int64_t)b * D.Hq * d +
                   (int64_t)g * GRP * d;
-  for (int o = tid; o < GRP * d; o += kConsumers) {
-    const int h = o / d, i = o - h * d;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w)
-      M = fmaxf(M, wbuf[(w * GRP + h) * rec]);
-    float Ls = 0.f, A = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float* r = wbuf + (w * GRP + h) * rec;
-      const float sc = (r[0] == -INFINITY) ? 0.f : expf(r[0] - M);
-      Ls = fmaf(r[1], sc, Ls);
-      A = fmaf(r[2 + i], sc, A);
-    }
-    out[o] = f2bf(A / Ls);
-  }
+  merge_warps<GRP, d>(S, wbuf, [=](int h, int i, float A, float Ls, float) {
+    out[h * d + i] = f2bf(A / Ls);
+  });
+}
+
+// JIT attention tasks (batch > 1) as a separate function: its paged-cache
+// reads need registers of their own, which would otherwise spill around
+// every other task body of the kernel.
+template <int DL, int GRP>
+__device__ __noinline__ void attn_body_jit(const KernelParams& P,
+                                           const Smem& S, const TaskDesc& t,
+                                           Ring& ring, uint64_t deadline) {
+  attn_body<DL, GRP, false>(P, S, t, ring, deadline);
 }
 
 __device__ void task_attn(const KernelParams& P, const Smem& S,
                           const TaskDesc& t, Ring& ring, uint64_t deadline) {
   const int grp = P.dims.Hq / P.dims.Hkv;
   const int dl = P.dims.d / 32;
-#define MPK_ATTN_CASE(G)                                   \
-  if (grp == G) {                                          \
-    if (dl == 4) attn_body<4, G>(P, S, t, ring, deadline); \
-    else if (dl == 2) attn_body<2, G>(P, S, t, ring, deadline); \
-    else attn_body<1, G>(P, S, t, ring, deadline);         \
-    return;                                                \
+  const bool pre = t.launch == MPK_LAUNCH_AOT;
+#define MPK_ATTN_CASE(G, DL)                                     \
+  if (grp == G && dl == DL) {                                    \
+    if (pre) attn_body<DL, G, true>(P, S, t, ring, deadline);    \
+    else attn_body_jit<DL, G>(P, S, t, ring, deadline);          \
+    return;                                                      \
   }
-  MPK_ATTN_CASE(1)
-  MPK_ATTN_CASE(2)
-  MPK_ATTN_CASE(4)
-  MPK_ATTN_CASE(8)
+  MPK_ATTN_CASE(1, 1) MPK_ATTN_CASE(1, 2) MPK_ATTN_CASE(1, 4)
+  MPK_ATTN_CASE(2, 1) MPK_ATTN_CASE(2, 2) MPK_ATTN_CASE(2, 4)
+  MPK_ATTN_CASE(4, 1) MPK_ATTN_CASE(4, 2) MPK_ATTN_CASE(4, 4)
+  MPK_ATTN_CASE(8, 1) MPK_ATTN_CASE(8, 2) MPK_ATTN_CASE(8, 4)
 #undef MPK_ATTN_CASE
   if (threadIdx.x == 0) raise_error(P, MPK_ERR_UNSUPPORTED);
 }

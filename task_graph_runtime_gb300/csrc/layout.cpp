@@ -42,7 +42,8 @@ bool smem_layout(const BuiltGraph& bg, int pages_req, int limit,
     L.bars = off;
     off = round_up(off + 16 * pages, 128);
     L.ctrl = off;
-    off += 384;   // control words, staged descriptors and records, times
+    off += 448;   // control words, staged descriptors and records, times,
+                  // attention positions per ring slot
     L.scratch = off;
     off += 512;
     L.total = off;
