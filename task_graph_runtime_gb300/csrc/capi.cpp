@@ -126,6 +126,18 @@ bool encode(mpk_graph* g) {
     r.id = g->h_aot[i];
     r.dep_count = g->h_events[r.desc.dep].count;
     r.trig_ev = g->h_events[r.desc.trig];
+    r.fan[0] = r.fan[1] = -1;
+    const EventDesc& e = r.trig_ev;
+    const int n_in = (int)(e.flags >> kEvInlineShift);
+    bool cached = !(e.flags & EV_HAS_JIT) && (e.flags & EV_HAS_INLINE) &&
+                  n_in == e.last - e.first + 1 && n_in <= 2;
+    for (int k = 0; cached && k < n_in; ++k) {
+      const int f = g->h_tasks[e.first + k].trig;
+      if (g->h_events[f].flags != 0) cached = false;
+      r.fan[k] = f;
+    }
+    if (cached) r.trig_ev.flags |= EV_FAN_CACHED;
+    else r.fan[0] = r.fan[1] = -1;
   }
   g->h_op_tasks.clear();
   g->h_op_first.clear();
@@ -503,7 +515,7 @@ mpk_status mpk_debug_add_event_count(mpk_graph* g, int event, int delta) {
   // the AOT records carry copies of their wait and trigger events' counts
   for (AotRec& r : g->h_aot_rec) {
     if (r.desc.dep == event) r.dep_count = g->h_events[event].count;
-    if (r.desc.trig == event) r.trig_ev = g->h_events[event];
+    if (r.desc.trig == event) r.trig_ev.count = g->h_events[event].count;
   }
   if (g->bound) {
     CK(cudaMemcpy(g->d_events.p + event, &g->h_events[event],

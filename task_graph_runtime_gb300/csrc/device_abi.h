@@ -33,7 +33,7 @@ enum : uint8_t { TASK_F_RESIDUAL = 1u };
 // Event flags.  Empty (inline) tasks get the highest ids and BFS appends
 // an event's dependent tasks in ascending id, so an event's inline tasks are
 // the last n of [first, last]; n is stored in bits 8..31.
-enum : uint32_t { EV_HAS_JIT = 1u, EV_HAS_INLINE = 2u };
+enum : uint32_t { EV_HAS_JIT = 1u, EV_HAS_INLINE = 2u, EV_FAN_CACHED = 4u };
 constexpr int kEvInlineShift = 8;
 
 // 16-byte event descriptor: activated when its counter reaches
@@ -50,11 +50,17 @@ static_assert(sizeof(EventDesc) == 16, "event descriptor must stay 16 bytes");
 // the task: the descriptor, the count its dependent event reaches per step,
 // and its triggering event.  Fetched asynchronously while the task before
 // it runs, so dispatch and trigger make no dependent global loads.
+// When every dependent task of the triggering event is an empty (inline)
+// task, there are at most two of them and each triggers an event with no
+// JIT or inline work of its own, trig_ev.flags carries EV_FAN_CACHED and
+// fan[] holds those events: the trigger then fires them without reading the
+// graph (and, for an event with one trigger, without touching its counter,
+// which nothing else reads).
 struct AotRec {
   TaskDesc desc;
   uint32_t dep_count;
   int32_t id;          // linear task id
-  uint32_t pad[2];
+  int32_t fan[2];
   EventDesc trig_ev;
 };
 static_assert(sizeof(AotRec) == 64, "AOT record must stay 64 bytes");

@@ -272,11 +272,12 @@ struct Smem {
   uint64_t* empty;
   volatile int* ctrl; // [0..1] command, [2] bail-out, [3] aborted at entry,
                       // [4] last-chunk flag, [8..10] leader loop state
-  TaskDesc* desc;     // [0..1] staged descriptors
+  TaskDesc* desc;     // [0..1] staged descriptors (slot 2: the fan below)
   uint64_t* times;    // trace: [0] looked-for, [1] ready, [2] operands
                       // staged, [3] last page consumed, [4] body done
   AotRec* head;       // [2] the head AOT record (by queue position parity)
   EventDesc* tev;     // [0..1] triggering event of the staged task
+  int32_t* fan;       // [0..1][2] cached fan-out events of the staged task
   int2* meta;         // [ring slot] (position, new token's KV page) of the
                       // AOT attention task whose K page is in that slot
   float* scratch;
@@ -297,6 +298,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const SmemLayout& L) {
   s.head = reinterpret_cast<AotRec*>(base + L.ctrl + 224);
   s.tev = reinterpret_cast<EventDesc*>(base + L.ctrl + 352);
   s.meta = reinterpret_cast<int2*>(base + L.ctrl + 384);
+  s.fan = reinterpret_cast<int32_t*>(base + L.ctrl + 128);
   s.scratch = reinterpret_cast<float*>(base + L.scratch);
   s.n_pages = L.n_pages;
   s.page_bytes = L.page_bytes;
@@ -1744,28 +1746,39 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
 #pragma unroll
       for (int e = 0; e < DL; ++e) Aw[h][e] = 0.f;
     }
+    // J chunks' partials are loaded before any is merged, so their global
+    // reads overlap
+    constexpr int J = GRP * (2 + DL) <= 24 ? 3 : 1;
 #pragma unroll 1
-    for (int c = warp; c < C; c += kConsumerWarps) {
-      const float* rc = part + (int64_t)c * GRP * rec;
-      float mc[GRP], lc[GRP], ac[GRP][DL];
+    for (int c0 = warp; c0 < C; c0 += J * kConsumerWarps) {
+      float mc[J][GRP], lc[J][GRP], ac[J][GRP][DL];
 #pragma unroll
-      for (int h = 0; h < GRP; ++h) {
-        mc[h] = __ldcg(rc + h * rec);
-        lc[h] = __ldcg(rc + h * rec + 1);
+      for (int j = 0; j < J; ++j) {
+        const int c = c0 + j * kConsumerWarps;
+        const float* rc = part + (int64_t)min(c, C - 1) * GRP * rec;
 #pragma unroll
-        for (int e = 0; e < DL; ++e)
-          ac[h][e] = __ldcg(rc + h * rec + 2 + lane * DL + e);
+        for (int h = 0; h < GRP; ++h) {
+          mc[j][h] = c < C ? __ldcg(rc + h * rec) : -INFINITY;
+          lc[j][h] = __ldcg(rc + h * rec + 1);
+#pragma unroll
+          for (int e = 0; e < DL; ++e)
+            ac[j][h][e] = __ldcg(rc + h * rec + 2 + lane * DL + e);
+        }
       }
 #pragma unroll
-      for (int h = 0; h < GRP; ++h) {
-        const float Mn = fmaxf(Mw[h], mc[h]);
-        if (Mn == -INFINITY) continue;
-        const float sa = (Mw[h] == -INFINITY) ? 0.f : expf(Mw[h] - Mn);
-        const float sc = (mc[h] == -INFINITY) ? 0.f : expf(mc[h] - Mn);
-        Lw[h] = Lw[h] * sa + lc[h] * sc;
+      for (int j = 0; j < J; ++j) {
 #pragma unroll
-        for (int e = 0; e < DL; ++e) Aw[h][e] = Aw[h][e] * sa + ac[h][e] * sc;
-        Mw[h] = Mn;
+        for (int h = 0; h < GRP; ++h) {
+          const float Mn = fmaxf(Mw[h], mc[j][h]);
+          if (Mn == -INFINITY) continue;
+          const float sa = (Mw[h] == -INFINITY) ? 0.f : expf(Mw[h] - Mn);
+          const float sc = (mc[j][h] == -INFINITY) ? 0.f : expf(mc[j][h] - Mn);
+          Lw[h] = Lw[h] * sa + lc[j][h] * sc;
+#pragma unroll
+          for (int e = 0; e < DL; ++e)
+            Aw[h][e] = Aw[h][e] * sa + ac[j][h][e] * sc;
+          Mw[h] = Mn;
+        }
       }
     }
     consumer_sync();   // wbuf and the scratch factors are reused
@@ -1923,9 +1936,18 @@ __device__ __forceinline__ bool ring_try_pop(RingHdr* hdr, uint64_t* slots,
 // tasks, and runs its empty tasks inline (they only trigger their own
 // event, whose descriptor is read from the graph).
 __device__ void trigger(const KernelParams& P, int e, const EventDesc& ed0,
-                        uint64_t deadline) {
+                        const int32_t* fan, uint64_t deadline) {
   const DevGraph& G = P.graph;
   const uint32_t epoch = P.step.epoch;
+  if (ed0.flags & EV_FAN_CACHED) {
+    bool fire = ed0.count == 1;
+    if (!fire) fire = atom_acq_rel_add(G.counters + e, 1u) + 1u == epoch * ed0.count;
+    if (fire) {
+      red_release_add(G.counters + fan[0], 1u);
+      if (fan[1] >= 0) red_release_add(G.counters + fan[1], 1u);
+    }
+    return;
+  }
   int stack[16];
   int sp = 0;
   int ev = e;
@@ -2026,6 +2048,7 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
           cmd = (int)v;
           S.desc[slot] = G.tasks[cmd];
           S.tev[slot] = G.events[S.desc[slot].trig];
+          S.fan[2 * slot] = S.fan[2 * slot + 1] = -1;
           break;
         }
         // the acquire orders this CTA's later reads after the producers'
@@ -2036,6 +2059,8 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
             cmd = hr->id;
             S.desc[slot] = hr->desc;
             S.tev[slot] = hr->trig_ev;
+            S.fan[2 * slot] = hr->fan[0];
+            S.fan[2 * slot + 1] = hr->fan[1];
             *ai_s = ai + 1;
             if (ai + 1 < *a1_s)
               fetch_rec(G.aot_rec + ai + 1, &S.head[(ai + 1) & 1]);
@@ -2072,7 +2097,7 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
       // the red.release / atom.acq_rel of the trigger is cumulative: it
       // orders every write of the CTA that the barrier above ordered before
       // this thread
-      trigger(P, S.desc[slot].trig, S.tev[slot], deadline);
+      trigger(P, S.desc[slot].trig, S.tev[slot], S.fan + 2 * slot, deadline);
       if (G.trace) {
         // (task | worker << 32), looked-for, ready, staged, pages done,
         // body done, triggered
