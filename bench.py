@@ -438,18 +438,24 @@ def run_ours(args, rank, world, local_rank):
 
 
 def load_traffic(workload, mode):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else null)."""
+    """DRAM bytes per launch from the committed ncu summary
+    profiles/traffic_<workload>_<mode>.txt ("key: value" lines), if it was
+    taken on the current kernel source (else null)."""
     import hashlib
-    p = os.path.join(ROOT, "profiles", f"traffic_{workload}_{mode}.json")
+    p = os.path.join(ROOT, "profiles", f"traffic_{workload}_{mode}.txt")
     src = os.path.join(ROOT, "task_graph_runtime_gb300", "csrc", "kernels.cu")
     if not os.path.exists(p):
         return None
+    d = {}
     with open(p) as f:
-        d = json.load(f)
+        for line in f:
+            if ":" in line and not line.startswith(("#", " ", "|")):
+                k, v = line.split(":", 1)
+                d[k.strip()] = v.strip()
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return d.get("dram_bytes_per_launch") if d.get("kernels_sha") == h \
-        else None
+    if d.get("kernels_sha") != h or "dram_bytes_per_launch" not in d:
+        return None
+    return int(float(d["dram_bytes_per_launch"]))
 
 
 def run_reference(args):

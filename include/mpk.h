@@ -79,8 +79,12 @@ typedef struct {
   int gemv_rows_per_task; /* MatMul output rows per task at batch < 8 (a
                              multiple of 8).  0: T = W * ceil(ceil(N/cap)/W)
                              tiles (at most ceil(N/8)) of multiples of 8
-                             rows, cap = 2048 page rows at batch 1 and 64 at
-                             batch 2..7 (a gate/up row counts twice)        */
+                             rows (single rows at batch 1).  cap at batch 1:
+                             2560 / p rows, p = the partial sums a row's dot
+                             product is split into (1 when a 32 KB page
+                             holds r = max(1, 16384 / K) >= 8 rows, else
+                             8 / r); 64 at batch 2..7; a gate/up row counts
+                             twice; rounded down to a multiple of 8        */
   int mma_rows_per_task;  /* the same for batch >= 8, where MatMul tiles run
                              on tensor cores; 0: as above with cap = 128    */
   int attn_chunks;        /* split-KV chunks per (sequence, KV head).  0:
@@ -88,8 +92,9 @@ typedef struct {
                              ceil(4W/(batch*n_kv_heads))))                  */
   int num_sched_sms;      /* SMs running scheduler warps. 0: 4 (Table 1)    */
   int sched_warps_per_sm; /* 0: 4 (Table 1)                                 */
-  int smem_pages;         /* weight pages (8 rows x 2048 columns, 32 KB +
-                             row skew) per worker. 0: as many as fit, <= 6  */
+  int smem_pages;         /* weight pages per worker (batch 1: 32 KB of
+                             whole rows; batch > 1: 8 rows x 2048 columns,
+                             32 KB + row skew). 0: as many as fit, <= 6    */
   int coarse_events;      /* 1: every task of an operator waits for every
                              task of the operators it reads (the
                              operator-level graph of Figure 4c, an
@@ -278,9 +283,10 @@ mpk_status mpk_debug_read_hidden(mpk_graph* g, int layer, uint16_t* host_out);
  * latency-critical loop that may not take the device-wide synchronisation
  * cudaMalloc/cudaFree imply, or a plugin whose host owns every allocation.
  * The call runs the kernel-per-operator form of the step (the same task
- * bodies as mpk_decode_step) and keeps all of its scratch -- descriptors,
- * TMA descriptors, the RoPE table, the activation workspace and the status
- * word -- in one static device array of MPK_NOALLOC_SCRATCH_BYTES that every
+ * bodies as mpk_decode_step) and keeps all of its scratch -- task
+ * descriptors, the layer pointer table, the RoPE table, the attention merge
+ * counters, the activation workspace and the status words -- in one static
+ * device array of MPK_NOALLOC_SCRATCH_BYTES that every
  * GPU loading the library holds until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *
