@@ -271,13 +271,15 @@ struct Smem {
   uint64_t* full;
   uint64_t* empty;
   volatile int* ctrl; // [0..1] command, [2] bail-out, [3] aborted at entry,
-                      // [4] last-chunk flag, [8..10] leader loop state
+                      // [4] last-chunk flag, [8..10] leader loop state,
+                      // [13] JIT stage barrier phases
   TaskDesc* desc;     // [0..1] staged descriptors (slot 2: the fan below)
   uint64_t* times;    // trace: [0] looked-for, [1] ready, [2] operands
                       // staged, [3] last page consumed, [4] body done
   AotRec* head;       // [2] the head AOT record (by queue position parity)
   EventDesc* tev;     // [0..1] triggering event of the staged task
   int32_t* fan;       // [0..1][2] cached fan-out events of the staged task
+  uint64_t* jit_bar;  // [2] JIT attention stage barriers
   int2* meta;         // [ring slot] (position, new token's KV page) of the
                       // AOT attention task whose K page is in that slot
   float* scratch;
@@ -299,6 +301,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const SmemLayout& L) {
   s.tev = reinterpret_cast<EventDesc*>(base + L.ctrl + 352);
   s.meta = reinterpret_cast<int2*>(base + L.ctrl + 384);
   s.fan = reinterpret_cast<int32_t*>(base + L.ctrl + 128);
+  s.jit_bar = reinterpret_cast<uint64_t*>(base + L.ctrl + 208);
   s.scratch = reinterpret_cast<float*>(base + L.scratch);
   s.n_pages = L.n_pages;
   s.page_bytes = L.page_bytes;
@@ -1448,33 +1451,131 @@ __device__ __forceinline__ void load_row_cg(const uint16_t* p, int DLc,
   }
 }
 
-// Row `tok` of the K (or V) chunk, this lane's DL values: from the ring
-// page (AOT) or the paged cache (JIT); zero past the chunk.
-template <int DL, bool PRE>
-__device__ __forceinline__ void attn_row(const KernelParams& P,
-                                         const uint8_t* page,
-                                         const uint16_t* pool, int tok,
-                                         int t0, int t1, int64_t layer_elems,
-                                         int64_t head_elems, const int32_t* pt,
+// This lane's DL values of a K (or V) row in shared memory, widened.
+template <int DL>
+__device__ __forceinline__ void smem_row(const uint16_t* row,
                                          float (&out)[DL]) {
-  const int lane = threadIdx.x & 31, d = DL * 32;
+  load_row(row + (threadIdx.x & 31) * DL, DL, out);
+}
+
+// Online softmax over the tokens [lo, hi) of one shared-memory buffer whose
+// row 0 is token `base` (K rows at kb, V rows at vb, d values each), in
+// blocks of 32/GRP tokens dealt to the 8 consumer warps (lane j of a block
+// scores token j/GRP against head j mod GRP).  The token `newpos` (when
+// >= 0) is read from knew/vnew instead.  Updates this warp's (m, l, acc).
+template <int DL, int GRP>
+__device__ __forceinline__ void attn_tokens(
+    const KernelParams& P, const float (&qr)[GRP][DL], const uint16_t* kb,
+    const uint16_t* vb, int base, int lo, int hi, int newpos,
+    const uint16_t* knew, const uint16_t* vnew, float& m_run, float& l_run,
+    float (&acc)[GRP][DL]) {
+  constexpr int d = DL * 32, TB = 32 / GRP;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nblk = (hi - lo + TB - 1) / TB;
+  for (int blk = warp; blk < nblk; blk += kConsumerWarps) {
+    const int t_blk = lo + blk * TB;
+    // scores: one K row at a time
+    float sv[32];
 #pragma unroll
-  for (int e = 0; e < DL; ++e) out[e] = 0.f;
-  if (tok >= t1) return;
-  if constexpr (PRE) {
-    load_row(reinterpret_cast<const uint16_t*>(page) + (size_t)(tok - t0) * d +
-                 lane * DL,
-             DL, out);
-  } else {
-    const Dims& D = P.dims;
-    const int page_id = __ldg(pt + tok / D.page_size);
-    if (page_id >= 0 && page_id < P.step.num_pages) {
-      load_row_cg(pool + layer_elems + (int64_t)page_id * D.Hkv * head_elems +
-                      (int64_t)(tok % D.page_size) * d + lane * DL,
-                  DL, out);
-    } else if (lane == 0) {
-      raise_error(P, MPK_ERR_KV_PAGE);
+    for (int tb = 0; tb < TB; ++tb) {
+      const int tok = t_blk + tb;
+      float kf[DL];
+#pragma unroll
+      for (int e = 0; e < DL; ++e) kf[e] = 0.f;
+      if (tok < hi)
+        smem_row<DL>(tok == newpos ? knew : kb + (size_t)(tok - base) * d, kf);
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        float sc = 0.f;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) sc = fmaf(qr[h][e], kf[e], sc);
+        sv[tb * GRP + h] = sc;
+      }
     }
+    float sc = reduce_scatter32(sv) * P.dims.attn_scale;
+    if (t_blk + lane / GRP >= hi) sc = -INFINITY;
+    float mb = sc;
+#pragma unroll
+    for (int o = GRP; o < 32; o <<= 1)
+      mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+    const float m_new = fmaxf(m_run, mb);   // finite: the block's token 0 is
+                                            // always valid
+    const float corr = (m_run == -INFINITY) ? 0.f : expf(m_run - m_new);
+    const float p = (sc == -INFINITY) ? 0.f : expf(sc - m_new);
+    float lb = p;
+#pragma unroll
+    for (int o = GRP; o < 32; o <<= 1) lb += __shfl_xor_sync(kFull, lb, o);
+    l_run = l_run * corr + lb;
+    m_run = m_new;
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+      const float ch = __shfl_sync(kFull, corr, h);
+#pragma unroll
+      for (int e = 0; e < DL; ++e) acc[h][e] *= ch;
+    }
+#pragma unroll
+    for (int tb = 0; tb < TB; ++tb) {
+      const int tok = t_blk + tb;
+      float vf[DL];
+#pragma unroll
+      for (int e = 0; e < DL; ++e) vf[e] = 0.f;
+      if (tok < hi)
+        smem_row<DL>(tok == newpos ? vnew : vb + (size_t)(tok - base) * d, vf);
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        const float pth = __shfl_sync(kFull, p, tb * GRP + h);
+#pragma unroll
+        for (int e = 0; e < DL; ++e) acc[h][e] = fmaf(pth, vf[e], acc[h][e]);
+      }
+    }
+  }
+}
+
+// JIT attention streams its cached tokens through two shared-memory stages
+// of kJitStageTok tokens (K rows then V rows), filled by bulk copies that
+// consumer thread 0 issues, one per run of tokens inside a KV page.
+constexpr int kJitStageTok = 64;
+__device__ __host__ __forceinline__ int jit_stage_bytes(int d) {
+  return kJitStageTok * d * 2 * 2;   // K and V rows of one stage
+}
+
+// Copy the cached tokens [a, e) of (layer l, sequence b, KV head g) into a
+// stage (K rows at kdst, V rows at vdst, row 0 = token a); completes on
+// `bar` (thread 0).  Unmapped pages raise MPK_ERR_KV_PAGE and are skipped
+// (their bytes are not expected, so the stage still completes).
+__device__ void issue_kv_stage(const KernelParams& P, int l, int b, int g,
+                               int a, int e, uint8_t* kdst, uint8_t* vdst,
+                               uint64_t* bar, uint64_t policy) {
+  const Dims& D = P.dims;
+  const int P_ = D.page_size, d = D.d;
+  const uint32_t row_bytes = (uint32_t)d * 2u;
+  const int32_t* pt = P.step.page_table + (int64_t)b * D.max_pages;
+  const int64_t head_elems = (int64_t)P_ * d;
+  const int64_t layer_elems = (int64_t)l * P.step.num_pages * D.Hkv * head_elems;
+  uint32_t total = 0;
+  for (int tok = a; tok < e;) {
+    const int run_end = min(e, (tok / P_ + 1) * P_);
+    const int pg = __ldg(pt + tok / P_);
+    if (pg >= 0 && pg < P.step.num_pages)
+      total += (uint32_t)(run_end - tok) * row_bytes * 2u;
+    else
+      raise_error(P, MPK_ERR_KV_PAGE);
+    tok = run_end;
+  }
+  mbar_arrive_expect_tx(bar, total);
+  for (int tok = a; tok < e;) {
+    const int run_end = min(e, (tok / P_ + 1) * P_);
+    const int pg = __ldg(pt + tok / P_);
+    if (pg >= 0 && pg < P.step.num_pages) {
+      const int64_t off = layer_elems + ((int64_t)pg * D.Hkv + g) * head_elems +
+                          (int64_t)(tok % P_) * d;
+      const uint32_t bytes = (uint32_t)(run_end - tok) * row_bytes;
+      bulk_g2s(kdst + (size_t)(tok - a) * row_bytes, P.step.k_pool + off,
+               bytes, bar, policy);
+      bulk_g2s(vdst + (size_t)(tok - a) * row_bytes, P.step.v_pool + off,
+               bytes, bar, policy);
+    }
+    tok = run_end;
   }
 }
 
@@ -1532,12 +1633,22 @@ __device__ __forceinline__ void merge_warps(const Smem& S, const float* wbuf,
 template <int DL, int GRP, bool PRE>
 __device__ void attn_body(const KernelParams& P, const Smem& S,
                           const TaskDesc& t, Ring& ring, uint64_t deadline) {
-  constexpr int d = DL * 32, TB = 32 / GRP, rec = 2 + d;
+  constexpr int d = DL * 32, rec = 2 + d;
   const Dims& D = P.dims;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = t.b, g = t.g, l = t.layer, C = D.C;
-  float* qf = reinterpret_cast<float*>(S.xs);       // [GRP][d]
-  float* wbuf = qf + GRP * d;                        // [8][GRP][2 + d]
+  // scratch: (JIT) two K/V stages | q [GRP][d] | warp records [8][GRP][rec]
+  // | (JIT) the new token's K and V rows (bf16)
+  uint8_t* stage0 = reinterpret_cast<uint8_t*>(S.xs);
+  float* qf = reinterpret_cast<float*>(stage0 + (PRE ? 0 : 2 * jit_stage_bytes(d)));
+  float* wbuf = qf + GRP * d;
+  uint16_t* knew = reinterpret_cast<uint16_t*>(wbuf + kConsumerWarps * GRP * rec);
+  uint16_t* vnew = knew + d;
+  if (!PRE && (int)(reinterpret_cast<uint8_t*>(vnew + d) - stage0) >
+                  P.sm.xs_bytes) {
+    if (tid == 0) raise_error(P, MPK_ERR_UNSUPPORTED);
+    return;
+  }
   bool have_k = true, have_v = true;
   uint8_t *kpage = nullptr, *vpage = nullptr;
   Ring kr = ring;
@@ -1607,15 +1718,16 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
                                  (hh == GRP ? kpage : vpage)) +
                                  (size_t)(pos - t0) * d
                            : nullptr;
+        uint16_t* mine = hh == GRP ? knew : vnew;
 #pragma unroll
         for (int e = 0; e < DL; ++e) {
           const uint16_t u = f2bf(x[e]);
           cache[lane * DL + e] = u;
           if (PRE) pg[lane * DL + e] = u;
+          else mine[lane * DL + e] = u;
         }
       }
     }
-    if (!PRE) __threadfence();   // the new K/V row is read back below
     consumer_sync();
   }
   stamp(P, S, 2);
@@ -1631,64 +1743,71 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
   for (int h = 0; h < GRP; ++h)
 #pragma unroll
     for (int e = 0; e < DL; ++e) acc[h][e] = 0.f;
-  const int64_t head_elems = (int64_t)D.page_size * d;
-  const int64_t layer_elems =
-      (int64_t)l * P.step.num_pages * D.Hkv * head_elems +
-      (int64_t)g * head_elems;
-  const int32_t* pt = P.step.page_table + (int64_t)b * D.max_pages;
-  const int ntok = t1 - t0;
-  const int nblk = (ntok + TB - 1) / TB;
-  for (int blk = warp; blk < nblk; blk += kConsumerWarps) {
-    // scores: one K row at a time
-    float sv[32];
-#pragma unroll
-    for (int tb = 0; tb < TB; ++tb) {
-      const int tok = t0 + blk * TB + tb;
-      float kf[DL];
-      attn_row<DL, PRE>(P, kpage, P.step.k_pool, tok, t0, t1, layer_elems,
-                        head_elems, pt, kf);
-#pragma unroll
-      for (int h = 0; h < GRP; ++h) {
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < DL; ++e) s = fmaf(qr[h][e], kf[e], s);
-        sv[tb * GRP + h] = s;
+  if constexpr (PRE) {
+    attn_tokens<DL, GRP>(P, qr, reinterpret_cast<const uint16_t*>(kpage),
+                         reinterpret_cast<const uint16_t*>(vpage), t0, t0, t1,
+                         -1, nullptr, nullptr, m_run, l_run, acc);
+  } else {
+    // cached tokens [t0, ce) come through the stages; the new token (if
+    // this chunk holds it) from knew/vnew
+    const int ce = has_new ? pos : t1;
+    const int nsub = (t1 - t0 + kJitStageTok - 1) / kJitStageTok;
+    const int sb = jit_stage_bytes(d) / 2;   // K (or V) rows of one stage
+    uint64_t* sbar = S.jit_bar;
+    uint32_t ph = (uint32_t)S.ctrl[13];
+    const uint64_t policy = evict_first_policy();
+    // thread 0: fills issued and not yet seen complete (bit per stage), and
+    // the phase each of them completes
+    uint32_t pend = 0, pend_ph = 0;
+    if (tid == 0) {
+      for (int s = 0; s < 2 && s < nsub; ++s) {
+        const int a = t0 + s * kJitStageTok;
+        issue_kv_stage(P, l, b, g, a, min(ce, a + kJitStageTok),
+                       stage0 + s * 2 * sb, stage0 + s * 2 * sb + sb,
+                       &sbar[s], policy);
+        pend |= 1u << s;
+        pend_ph = (pend_ph & ~(1u << s)) | (ph & (1u << s));
       }
     }
-    float s = reduce_scatter32(sv) * D.attn_scale;
-    const int my_tok = t0 + blk * TB + lane / GRP;
-    if (my_tok >= t1) s = -INFINITY;
-    float mb = s;
-#pragma unroll
-    for (int o = GRP; o < 32; o <<= 1)
-      mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
-    const float m_new = fmaxf(m_run, mb);   // finite: the block's token 0 is
-                                            // always valid
-    const float corr = (m_run == -INFINITY) ? 0.f : expf(m_run - m_new);
-    const float p = (s == -INFINITY) ? 0.f : expf(s - m_new);
-    float lb = p;
-#pragma unroll
-    for (int o = GRP; o < 32; o <<= 1) lb += __shfl_xor_sync(kFull, lb, o);
-    l_run = l_run * corr + lb;
-    m_run = m_new;
-#pragma unroll
-    for (int h = 0; h < GRP; ++h) {
-      const float ch = __shfl_sync(kFull, corr, h);
-#pragma unroll
-      for (int e = 0; e < DL; ++e) acc[h][e] *= ch;
-    }
-#pragma unroll
-    for (int tb = 0; tb < TB; ++tb) {
-      const int tok = t0 + blk * TB + tb;
-      float vf[DL];
-      attn_row<DL, PRE>(P, vpage, P.step.v_pool, tok, t0, t1, layer_elems,
-                        head_elems, pt, vf);
-#pragma unroll
-      for (int h = 0; h < GRP; ++h) {
-        const float pth = __shfl_sync(kFull, p, tb * GRP + h);
-#pragma unroll
-        for (int e = 0; e < DL; ++e) acc[h][e] = fmaf(pth, vf[e], acc[h][e]);
+    for (int s = 0; s < nsub; ++s) {
+      const int st = s & 1;
+      bool got = !S.ctrl[2];
+      uint32_t spins = 0;
+      while (got && !mbar_try_wait(&sbar[st], (ph >> st) & 1u)) {
+        if ((++spins & 1023u) == 0u && (aborted(P) || globaltimer() > deadline)) {
+          if (!aborted(P)) raise_error(P, MPK_ERR_TIMEOUT);
+          S.ctrl[2] = 1;
+          got = false;
+        }
       }
+      if (got) pend &= ~(1u << st);
+      ph ^= 1u << st;
+      const int lo = t0 + s * kJitStageTok, hi = min(t1, lo + kJitStageTok);
+      if (got)
+        attn_tokens<DL, GRP>(
+            P, qr, reinterpret_cast<const uint16_t*>(stage0 + st * 2 * sb),
+            reinterpret_cast<const uint16_t*>(stage0 + st * 2 * sb + sb), lo,
+            lo, hi, has_new ? pos : -1, knew, vnew, m_run, l_run, acc);
+      consumer_sync();   // the stage is free again
+      if (tid == 0 && s + 2 < nsub && !S.ctrl[2]) {
+        const int a = lo + 2 * kJitStageTok;
+        issue_kv_stage(P, l, b, g, a, min(ce, a + kJitStageTok),
+                       stage0 + st * 2 * sb, stage0 + st * 2 * sb + sb,
+                       &sbar[st], policy);
+        pend |= 1u << st;
+        pend_ph = (pend_ph & ~(1u << st)) | (ph & (1u << st));
+      }
+    }
+    if (tid == 0) {
+      // an abandoned fill still completes (its bytes were expected): wait
+      // (bounded) so that no copy lands in shared memory after the task
+      const uint64_t lim = globaltimer() + 200000000ull;
+      for (int st = 0; st < 2; ++st)
+        if (pend & (1u << st))
+          while (!mbar_try_wait(&sbar[st], (pend_ph >> st) & 1u) &&
+                 globaltimer() < lim) {
+          }
+      S.ctrl[13] = (int)ph;
     }
   }
   stamp(P, S, 3);
@@ -2182,6 +2301,9 @@ __device__ __forceinline__ bool setup_smem(const KernelParams& P, uint8_t* raw,
     // mpk_reset; read it once per CTA so all threads agree
     S.ctrl[3] = aborted(P) ? 1 : 0;
     S.ctrl[4] = 0;
+    mbar_init(&S.jit_bar[0], 1);
+    mbar_init(&S.jit_bar[1], 1);
+    S.ctrl[13] = 0;   // JIT stage barrier phases
     fence_proxy_async_smem();
   }
   __syncthreads();

@@ -22,8 +22,12 @@ bool smem_layout(const BuiltGraph& bg, int pages_req, int limit,
   int xs = B == 1 ? round_up(kmax * 4, 16) : B * kPagePitch;   // fp32 x at B=1
   if (!chain) {
     const int grp = s.n_q_heads / s.n_kv_heads, d = s.head_dim;
-    const int attn = (grp * d + 2 * d + 8 * grp * (2 + d)) * 4;
-    xs = std::max(xs, attn);
+    // query rows + 8 warp records (+ the new K/V rows)
+    int attn = (grp * d + 8 * grp * (2 + d)) * 4 + 2 * d * 2;
+    const int max_ctx = s.max_pages_per_seq * s.page_size;
+    if (!attn_is_aot(B, max_ctx, bg.cfg.attn_chunks))
+      attn += 2 * 64 * d * 2 * 2;   // two K/V stages of 64 tokens (JIT)
+    xs = std::max(xs, round_up(attn, 16));
   }
   const int res_floats = B == 1 ? kB1Partials : B * (B < 8 ? 64 : 128);
   const int page_bytes = B == 1 ? kContigPageBytes : kPageBytes;
