@@ -275,6 +275,31 @@ mpk_status mpk_debug_read_trace(mpk_graph* g, uint64_t* host_records,
  * its RMSNorm prologue.  Decoder mode only. */
 mpk_status mpk_debug_read_hidden(mpk_graph* g, int layer, uint16_t* host_out);
 
+/* CPU model of the runtime protocol (no GPU needed).  Runs `steps` steps
+ * of g's own device encoding with one host thread per worker leader and per
+ * scheduler warp: epoch counters, AOT queues in linear order (with the
+ * cached fan-outs of the AOT records), JIT dispatch through scheduler and
+ * worker rings, and empty tasks run inline by the activating trigger, as
+ * the kernel does (MPK summary, §2 Q2 runtime; Figure 8).  Task bodies
+ * are replaced by random delays of 0..max_delay_us microseconds (seeded).
+ * Reports, in *report: executions, executions that started before some
+ * task triggering their event had finished in the same step, duplicate and
+ * missing executions per completed step, and whether a step failed to
+ * finish within timeout_ms (a deadlock).  Returns MPK_ERR_INVALID_ARG for
+ * bad arguments; the verdict is in the report. */
+typedef struct {
+  int64_t tasks_run;
+  int64_t order_violations;
+  int64_t duplicate_runs;
+  int64_t missing_runs;
+  int32_t deadlocked;
+  int32_t steps_completed;
+  double seconds;
+} mpk_sim_report;
+mpk_status mpk_debug_simulate(const mpk_graph* g, int steps, uint32_t seed,
+                              int max_delay_us, int timeout_ms,
+                              mpk_sim_report* report);
+
 /* Allocation-free decode step.  (The paper has no counterpart: this is a
  * convenience for callers of the library.)
  *

@@ -58,6 +58,9 @@ def build(verbose: bool = False) -> str:
         ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-c",
          os.path.join(CSRC, "layout.cpp"), "-o",
          os.path.join(BUILD_DIR, "layout.o")] + inc,
+        ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-pthread", "-c",
+         os.path.join(CSRC, "protocol_sim.cpp"), "-o",
+         os.path.join(BUILD_DIR, "protocol_sim.o")] + inc,
     ]
     with concurrent.futures.ThreadPoolExecutor(len(jobs)) as ex:
         for out in ex.map(_run, jobs):
@@ -70,6 +73,8 @@ def build(verbose: bool = False) -> str:
                           os.path.join(BUILD_DIR, "capi.o"),
                           os.path.join(BUILD_DIR, "tgraph_builder.o"),
                           os.path.join(BUILD_DIR, "layout.o"),
+                          os.path.join(BUILD_DIR, "protocol_sim.o"),
+                          "-Xcompiler", "-pthread",
                           "-Xlinker", "-rpath=" + os.path.join(cuda, "lib64")])
     os.replace(tmp, OUT)
     return OUT

@@ -74,6 +74,16 @@ class _KVCache(ctypes.Structure):
 _P32 = ctypes.POINTER(ctypes.c_int32)
 
 
+class SimReport(ctypes.Structure):
+    _fields_ = [("tasks_run", ctypes.c_int64),
+                ("order_violations", ctypes.c_int64),
+                ("duplicate_runs", ctypes.c_int64),
+                ("missing_runs", ctypes.c_int64),
+                ("deadlocked", ctypes.c_int32),
+                ("steps_completed", ctypes.c_int32),
+                ("seconds", ctypes.c_double)]
+
+
 class GraphExport(ctypes.Structure):
     _fields_ = [("n_tasks", ctypes.c_int), ("n_events", ctypes.c_int),
                 ("n_ops", ctypes.c_int), ("n_empty", ctypes.c_int),
@@ -119,6 +129,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mpk_debug_set_trace": ([vp, i], st),
         "mpk_debug_read_trace": ([vp, vp, i, ctypes.POINTER(i)], st),
         "mpk_debug_read_hidden": ([vp, i, vp], st),
+        "mpk_debug_simulate": ([vp, i, ctypes.c_uint32, i, i,
+                                ctypes.POINTER(SimReport)], st),
         "mpk_decode_step_noalloc": ([vp, ctypes.POINTER(_Weights), vp,
                                      ctypes.POINTER(_KVCache), vp, vp, vp,
                                      vp], st),
@@ -306,6 +318,17 @@ class Graph:
             self.handle, buf.ctypes.data, capacity, ctypes.byref(n)),
             "mpk_debug_read_trace")
         return buf[:n.value]
+
+    def simulate(self, steps: int = 2, seed: int = 0, max_delay_us: int = 20,
+                 timeout_ms: int = 20000) -> Dict[str, float]:
+        """CPU model of the runtime protocol on this graph's encoding
+        (mpk_debug_simulate): host threads for workers and scheduler warps,
+        random task delays."""
+        rep = SimReport()
+        _check(load_library().mpk_debug_simulate(
+            self.handle, steps, seed, max_delay_us, timeout_ms,
+            ctypes.byref(rep)), "mpk_debug_simulate")
+        return {k: getattr(rep, k) for k, _ in SimReport._fields_}
 
     def read_hidden(self, layer: int) -> np.ndarray:
         """bf16 bits [batch, hidden] of the residual stream entering decoder
