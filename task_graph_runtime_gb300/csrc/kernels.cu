@@ -785,34 +785,45 @@ __device__ __forceinline__ void prefetch_gain(const KernelParams& P,
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off) : "memory");
 }
 
-// Pre-norm values of 8 columns [k, k + 8) of sequence b.
-__device__ __forceinline__ void pre_values(const KernelParams& P,
-                                           const XSrc& x, int b, int K, int k,
+// Pre-norm values of 8 columns [k, k + 8) of sequence b from the raw words
+// of the source(s): the embedding row, or the two addends of the residual
+// sum (rounded to bf16, as the tensor is).
+struct PreRaw {
+  uint4 a, c;
+};
+__device__ __forceinline__ void pre_finish(const XSrc& x, const PreRaw& r,
                                            float (&v)[8]) {
+  const uint32_t* pa = &r.a.x;
+  const uint32_t* pc = &r.c.x;
   if (x.mode == X_NORM_EMBED) {
-    int tok = __ldg(P.step.tokens + b);
-    tok = min(max(tok, 0), P.dims.V - 1);
-    const uint4 e = __ldg(reinterpret_cast<const uint4*>(
-        P.w.embed + (int64_t)tok * K + k));
-    const uint32_t* pe = &e.x;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      v[2 * q] = bf_lo(pe[q]);
-      v[2 * q + 1] = bf_hi(pe[q]);
+      v[2 * q] = bf_lo(pa[q]);
+      v[2 * q + 1] = bf_hi(pa[q]);
     }
   } else {
-    const uint4 va =
-        __ldcg(reinterpret_cast<const uint4*>(x.a + (int64_t)b * K + k));
-    const uint4 vc =
-        __ldcg(reinterpret_cast<const uint4*>(x.c + (int64_t)b * K + k));
-    const uint32_t* pa = &va.x;
-    const uint32_t* pc = &vc.x;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       v[2 * q] = round_bf(__fadd_rn(bf_lo(pa[q]), bf_lo(pc[q])));
       v[2 * q + 1] = round_bf(__fadd_rn(bf_hi(pa[q]), bf_hi(pc[q])));
     }
   }
+}
+__device__ __forceinline__ void pre_values(const KernelParams& P,
+                                           const XSrc& x, int b, int K, int k,
+                                           float (&v)[8]) {
+  PreRaw r;
+  if (x.mode == X_NORM_EMBED) {
+    int tok = __ldg(P.step.tokens + b);
+    tok = min(max(tok, 0), P.dims.V - 1);
+    r.a = __ldg(reinterpret_cast<const uint4*>(P.w.embed + (int64_t)tok * K +
+                                               k));
+    r.c = make_uint4(0, 0, 0, 0);
+  } else {
+    r.a = __ldcg(reinterpret_cast<const uint4*>(x.a + (int64_t)b * K + k));
+    r.c = __ldcg(reinterpret_cast<const uint4*>(x.c + (int64_t)b * K + k));
+  }
+  pre_finish(x, r, v);
 }
 __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
   return make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]),
@@ -834,24 +845,13 @@ __device__ __forceinline__ float rms_factor(float ss, int K, float eps) {
   return 1.0f / sqrtf(ss / (float)K + eps);
 }
 
-// Batch 1: stage all K columns of x into S.xs as fp32 (the bf16 values,
-// widened exactly), so the MatMul loop converts only the weights.  Chunk c
-// (columns 8c .. 8c + 7) is split over two planes of float4 -- columns
-// 8c .. 8c + 3 at xs[c], 8c + 4 .. 8c + 7 at xs[nch + c] -- so that the
-// lanes of a warp read consecutive 16-byte words.
-__device__ __forceinline__ void store_f8(float4* xs, int nch, int c, uint4 v) {
-  const uint32_t* pv = &v.x;
-  float4 a, b;
-  a.x = bf_lo(pv[0]);
-  a.y = bf_hi(pv[0]);
-  a.z = bf_lo(pv[1]);
-  a.w = bf_hi(pv[1]);
-  b.x = bf_lo(pv[2]);
-  b.y = bf_hi(pv[2]);
-  b.z = bf_lo(pv[3]);
-  b.w = bf_hi(pv[3]);
-  xs[c] = a;
-  xs[nch + c] = b;
+// Batch 1: all K columns of x go to S.xs as bf16 (chunk c = columns
+// 8c .. 8c + 7 at 16-byte word c); the MatMul loop widens them once per tile
+// into registers, so the staging costs half the shared memory of fp32 and
+// leaves room for one more weight page.
+__device__ __forceinline__ void widen8(uint4 v, float4& a, float4& b) {
+  a = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
+  b = make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
 }
 
 __device__ void stage_x_b1(const KernelParams& P, const Smem& S,
@@ -859,10 +859,10 @@ __device__ void stage_x_b1(const KernelParams& P, const Smem& S,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const XSrc x = x_source(P, t);
   const int K = g.K, nch = K >> 3;
-  float4* xs = reinterpret_cast<float4*>(S.xs);
+  uint4* xs = reinterpret_cast<uint4*>(S.xs);
   if (x.mode == X_PLAIN) {
     for (int ch = tid; ch < nch; ch += kConsumers)
-      store_f8(xs, nch, ch, __ldcg(reinterpret_cast<const uint4*>(x.a) + ch));
+      xs[ch] = __ldcg(reinterpret_cast<const uint4*>(x.a) + ch);
     consumer_sync();
     return;
   }
@@ -891,7 +891,7 @@ __device__ void stage_x_b1(const KernelParams& P, const Smem& S,
   for (int k = 0; k < kMaxChunks; ++k) {
     const int ch = tid + k * kConsumers;
     if (ch < nch) {
-      store_f8(xs, nch, ch, norm8(v[k], r, wv[k]));
+      xs[ch] = norm8(v[k], r, wv[k]);
       if (x.resid) reinterpret_cast<uint4*>(x.resid)[ch] = pack8(v[k]);
     }
   }
@@ -899,25 +899,61 @@ __device__ void stage_x_b1(const KernelParams& P, const Smem& S,
 }
 
 // Batch > 1, norm modes: the RMS factor of every sequence into
-// S.scratch[32 + b] (one warp per sequence); tile 0 stores the residual.
+// S.scratch[32 + b] (warp w takes sequences w, w + 8, ...); tile 0 stores the
+// residual.  The input words are brought into the x buffer (not yet staged)
+// with asynchronous 16-byte copies, 1024 columns of every sequence at a
+// time, so all of a batch's loads are in flight together; each thread reads
+// back only the chunks it copied itself.
 __device__ void norm_stats(const KernelParams& P, const Smem& S,
                            const TaskDesc& t, const Gemv& g) {
   const XSrc x = x_source(P, t);
   if (x.mode == X_PLAIN) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int K = g.K, nch = K >> 3;
-  for (int b = warp; b < P.dims.B; b += kConsumerWarps) {
-    float ss = 0.f;
-    for (int ch = lane; ch < nch; ch += 32) {
-      float v[8];
-      pre_values(P, x, b, K, ch * 8, v);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
-      if (x.resid)
-        reinterpret_cast<uint4*>(x.resid + (int64_t)b * K)[ch] = pack8(v);
+  const int B = P.dims.B, K = g.K, nch = K >> 3;
+  constexpr int CB = 128;   // chunks (of 8 columns) per sequence per batch
+  uint4* ta = reinterpret_cast<uint4*>(S.xs);     // [B][CB]
+  uint4* tc = ta + (size_t)B * CB;                 // [B][CB]
+  float ss[2] = {0.f, 0.f};   // this lane's share for sequences warp, warp + 8
+  for (int c0 = 0; c0 < nch; c0 += CB) {
+    for (int q = 0; q < 2; ++q) {
+      const int b = warp + q * kConsumerWarps;
+      if (b >= B) break;
+      const uint16_t* ra;
+      if (x.mode == X_NORM_EMBED) {
+        int tok = __ldg(P.step.tokens + b);
+        tok = min(max(tok, 0), P.dims.V - 1);
+        ra = P.w.embed + (int64_t)tok * K;
+      } else {
+        ra = x.a + (int64_t)b * K;
+      }
+      for (int ch = lane; ch < CB && c0 + ch < nch; ch += 32) {
+        cp_async16(ta + b * CB + ch, ra + (c0 + ch) * 8);
+        if (x.mode != X_NORM_EMBED)
+          cp_async16(tc + b * CB + ch, x.c + (int64_t)b * K + (c0 + ch) * 8);
+      }
     }
-    ss = warp_sum(ss);
-    if (lane == 0) S.scratch[32 + b] = rms_factor(ss, K, P.dims.eps);
+    cp_async_commit();
+    cp_async_wait_all();
+    for (int q = 0; q < 2; ++q) {
+      const int b = warp + q * kConsumerWarps;
+      if (b >= B) break;
+      for (int ch = lane; ch < CB && c0 + ch < nch; ch += 32) {
+        PreRaw raw;
+        raw.a = ta[b * CB + ch];
+        raw.c = x.mode != X_NORM_EMBED ? tc[b * CB + ch] : make_uint4(0, 0, 0, 0);
+        float v[8];
+        pre_finish(x, raw, v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ss[q] = fmaf(v[k], v[k], ss[q]);
+        if (x.resid)
+          reinterpret_cast<uint4*>(x.resid + (int64_t)b * K)[c0 + ch] = pack8(v);
+      }
+    }
+  }
+  for (int q = 0; q < 2; ++q) {
+    const int b = warp + q * kConsumerWarps;
+    const float tot = warp_sum(ss[q]);
+    if (b < B && lane == 0) S.scratch[32 + b] = rms_factor(tot, K, P.dims.eps);
   }
   consumer_sync();
 }
@@ -941,13 +977,17 @@ __device__ void stage_x_seg(const KernelParams& P, const Smem& S,
     }
     const int k = c0 + ch * 8;
     if (x.mode == X_PLAIN) {
-      *dst = __ldcg(reinterpret_cast<const uint4*>(x.a + (int64_t)b * K + k));
+      cp_async16(dst, x.a + (int64_t)b * K + k);   // all in flight together
     } else {
       float v[8];
       pre_values(P, x, b, K, k, v);
       *dst = norm8(v, S.scratch[32 + b],
                    __ldg(reinterpret_cast<const uint4*>(x.gain + k)));
     }
+  }
+  if (x.mode == X_PLAIN) {
+    cp_async_commit();
+    cp_async_wait_all();
   }
   consumer_sync();
 }
@@ -1088,16 +1128,22 @@ __device__ __forceinline__ void fma8(uint4 w, float4 x0, float4 x1, float2& a,
   a = __ffma2_rn(make_float2(bf_lo(w.z), bf_hi(w.z)), make_float2(x1.x, x1.y), a);
   b = __ffma2_rn(make_float2(bf_lo(w.w), bf_hi(w.w)), make_float2(x1.z, x1.w), b);
 }
-__device__ __forceinline__ float row_dot(const uint4* row, const float4* xa,
-                                         const float4* xb, int c0, int c1) {
+__device__ __forceinline__ float row_dot(const uint4* row, const uint4* xs,
+                                         int c0, int c1) {
   const int lane = threadIdx.x & 31;
   float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
   int ch = c0 + lane;
+  float4 x0, x1, x2, x3;
   for (; ch + 32 < c1; ch += 64) {
-    fma8(row[ch], xa[ch], xb[ch], a0, a1);
-    fma8(row[ch + 32], xa[ch + 32], xb[ch + 32], a2, a3);
+    widen8(xs[ch], x0, x1);
+    widen8(xs[ch + 32], x2, x3);
+    fma8(row[ch], x0, x1, a0, a1);
+    fma8(row[ch + 32], x2, x3, a2, a3);
   }
-  if (ch < c1) fma8(row[ch], xa[ch], xb[ch], a0, a1);
+  if (ch < c1) {
+    widen8(xs[ch], x0, x1);
+    fma8(row[ch], x0, x1, a0, a1);
+  }
   return warp_sum(((a0.x + a0.y) + (a1.x + a1.y)) +
                   ((a2.x + a2.y) + (a3.x + a3.y)));
 }
@@ -1128,15 +1174,14 @@ template <int NCK>
 __device__ __forceinline__ void b1_page_rows(const uint4* pg, float* out,
                                              const Gemv& g, int i0, int n,
                                              bool multi, int part, int nch,
-                                             int c0, int c1, const float4* xa,
-                                             const float4* xb,
+                                             int c0, int c1, const uint4* xs,
                                              const float4 (&xr)[16]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (multi) {
     for (int r = warp; r < n; r += kConsumerWarps) {
       const uint4* row = pg + (size_t)r * nch;
       const float v = NCK > 0 ? row_dot_xreg<NCK>(row, xr)
-                              : row_dot(row, xa, xb, 0, nch);
+                              : row_dot(row, xs, 0, nch);
       if (lane == 0) out[i0 + r] = v;
     }
   } else {
@@ -1144,7 +1189,7 @@ __device__ __forceinline__ void b1_page_rows(const uint4* pg, float* out,
     if (r < n) {
       const uint4* row = pg + (size_t)r * nch;
       const float v = NCK > 0 ? row_dot_xreg<NCK>(row + c0, xr)
-                              : row_dot(row, xa, xb, c0, c1);
+                              : row_dot(row, xs, c0, c1);
       if (lane == 0) out[(i0 + r) * g.wpr + part] = v;
     }
   }
@@ -1161,14 +1206,11 @@ __device__ void gemv_b1_loop(const KernelParams& P, const Smem& S,
                              const Gemv& g, Ring& ring, uint64_t deadline,
                              bool multi, int part, int nch, int c0, int c1) {
   const int lane = threadIdx.x & 31;
-  const float4* xa = reinterpret_cast<const float4*>(S.xs);
-  const float4* xb = xa + nch;
+  const uint4* xs = reinterpret_cast<const uint4*>(S.xs);
   float4 xr[16];
 #pragma unroll
-  for (int k = 0; k < NCK; ++k) {
-    xr[2 * k] = xa[c0 + lane + 32 * k];
-    xr[2 * k + 1] = xb[c0 + lane + 32 * k];
-  }
+  for (int k = 0; k < NCK; ++k)
+    widen8(xs[c0 + lane + 32 * k], xr[2 * k], xr[2 * k + 1]);
   const int halves = g.dual ? 2 : 1;
   for (int half = 0; half < halves; ++half) {
     float* out = S.res + (size_t)half * g.rows * g.wpr;
@@ -1178,7 +1220,7 @@ __device__ void gemv_b1_loop(const KernelParams& P, const Smem& S,
       if (have)
         b1_page_rows<NCK>(
             reinterpret_cast<const uint4*>(page_ptr(S, ring.slot)), out, g,
-            i0, n, multi, part, nch, c0, c1, xa, xb, xr);
+            i0, n, multi, part, nch, c0, c1, xs, xr);
       release_page(S, ring, have);
     }
   }
@@ -1291,6 +1333,7 @@ __device__ void gemv_mma(const KernelParams& P, const Smem& S,
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int B = P.dims.B, RP = g.ngroups * kPageRows;
   norm_stats(P, S, t, g);
+  stamp(P, S, 2);
   float acc[2][2][4];
 #pragma unroll
   for (int a = 0; a < 2; ++a)
@@ -1337,6 +1380,7 @@ __device__ void gemv_mma(const KernelParams& P, const Smem& S,
     }
     skip_extra_groups(P, S, g, kMaxGroups, ring, deadline);
   }
+  stamp(P, S, 3);
   // D fragment: rows (sequences) lane/4 and lane/4 + 8, columns (page rows)
   // (lane % 4) * 2 and + 1
   const int bq = lane >> 2, nq = (lane & 3) * 2;

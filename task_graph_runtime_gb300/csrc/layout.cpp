@@ -19,7 +19,7 @@ bool smem_layout(const BuiltGraph& bg, int pages_req, int limit,
   const int kmax = chain ? std::max(s.hidden, s.chain_ffn)
                          : std::max({s.hidden, s.n_q_heads * s.head_dim,
                                      s.ffn});
-  int xs = B == 1 ? round_up(kmax * 4, 16) : B * kPagePitch;   // fp32 x at B=1
+  int xs = B == 1 ? round_up(kmax * 2, 16) : B * kPagePitch;   // bf16 x at B=1
   if (!chain) {
     const int grp = s.n_q_heads / s.n_kv_heads, d = s.head_dim;
     // query rows + 8 warp records (+ the new K/V rows)
@@ -49,7 +49,7 @@ bool smem_layout(const BuiltGraph& bg, int pages_req, int limit,
     off += 448;   // control words, staged descriptors and records, times,
                   // attention positions per ring slot
     L.scratch = off;
-    off += 512;
+    off += 384;   // reductions: <= 96 floats
     L.total = off;
     if (off <= limit) {
       *out = L;
