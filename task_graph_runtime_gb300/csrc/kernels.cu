@@ -2073,7 +2073,7 @@ __device__ bool ring_push(const KernelParams& P, RingHdr* hdr, uint64_t* slots,
                           uint32_t cap, uint32_t value, uint64_t deadline) {
   const uint32_t pos = atomicAdd(&hdr->tail, 1u);
   uint32_t spins = 0;
-  while (pos - ld_acquire(&hdr->head) >= cap) {
+  while ((int32_t)(pos - ld_acquire(&hdr->head)) >= (int32_t)cap) {
     if ((++spins & 255u) == 0u && (aborted(P) || globaltimer() > deadline)) {
       if (!aborted(P)) raise_error(P, MPK_ERR_QUEUE_OVERFLOW);
       return false;
