@@ -228,6 +228,22 @@ mpk_status mpk_decode_step(mpk_graph* g, const int32_t* d_tokens,
                            const mpk_kv_cache* kv, float* d_logits,
                            int32_t* d_next_tokens, void* cuda_stream);
 
+/* Several greedy steps in ONE launch (MPK summary, Figure 1: the whole
+ * decode loop inside a single launch).  Step i (0 <= i < n_steps) embeds
+ * d_tokens for i = 0, else the tokens step i - 1 wrote; it writes its own to
+ * d_next_tokens + i * batch (device int32 [n_steps][batch]).  d_logits
+ * receives the last step's logits.  kv and seq_lens advance by n_steps.
+ * Inside the kernel every worker walks its task queue once per step: the
+ * first tasks of step i + 1 wait for step i's end event, while the
+ * producers already stream step i + 1's weights during step i's last tasks
+ * (cached K/V pages only after that end event).  In the kernel-per-operator
+ * modes the steps are enqueued one after another.  Same errors and
+ * asynchrony as mpk_decode_step; n_steps < 1 is MPK_ERR_INVALID_ARG. */
+mpk_status mpk_decode_steps(mpk_graph* g, const int32_t* d_tokens,
+                            const mpk_kv_cache* kv, float* d_logits,
+                            int32_t* d_next_tokens, int n_steps,
+                            void* cuda_stream);
+
 /* Read the device status word of the last step.  Synchronises the device.
  * MPK_OK, or the first error the kernel latched. */
 mpk_status mpk_get_status(mpk_graph* g);

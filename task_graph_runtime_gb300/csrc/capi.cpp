@@ -416,7 +416,15 @@ static mpk_status enqueue_kpo(mpk_graph* g, cudaStream_t stream) {
 mpk_status mpk_decode_step(mpk_graph* g, const int32_t* d_tokens,
                            const mpk_kv_cache* kv, float* d_logits,
                            int32_t* d_next_tokens, void* cuda_stream) {
-  if (!g || !d_tokens || !d_logits || !d_next_tokens)
+  return mpk_decode_steps(g, d_tokens, kv, d_logits, d_next_tokens, 1,
+                          cuda_stream);
+}
+
+mpk_status mpk_decode_steps(mpk_graph* g, const int32_t* d_tokens,
+                            const mpk_kv_cache* kv, float* d_logits,
+                            int32_t* d_next_tokens, int n_steps,
+                            void* cuda_stream) {
+  if (!g || !d_tokens || !d_logits || !d_next_tokens || n_steps < 1)
     return MPK_ERR_INVALID_ARG;
   if (!g->bound) return MPK_ERR_NOT_BOUND;
   const mpk_model_shape& s = g->bg.cfg.shape;
@@ -426,6 +434,7 @@ mpk_status mpk_decode_step(mpk_graph* g, const int32_t* d_tokens,
   a.logits = d_logits;
   a.next_tokens = d_next_tokens;
   a.timeout_ns = g->timeout_ns;
+  a.n_steps = 1;
   if (!chain) {
     if (!kv || !kv->k_pool || !kv->v_pool || !kv->page_table ||
         !kv->seq_lens || kv->num_pages < 1 ||
@@ -440,7 +449,9 @@ mpk_status mpk_decode_step(mpk_graph* g, const int32_t* d_tokens,
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   CK(cudaSetDevice(g->device));
   if (g->mode == MPK_MODE_MEGAKERNEL) {
+    // one launch runs all n_steps steps (the loop lives in the kernel)
     a.epoch = g->epoch + 1;
+    a.n_steps = n_steps;
     g->params.step = a;
     const int grid = g->bg.cfg.num_workers + g->num_sched_sms;
     cudaError_t e = launch_megakernel(g->params, grid, g->smem, stream);
@@ -448,7 +459,18 @@ mpk_status mpk_decode_step(mpk_graph* g, const int32_t* d_tokens,
       cudaGetLastError();
       return cuda_status(e);
     }
-    g->epoch += 1;
+    g->epoch += (uint32_t)n_steps;
+    return MPK_OK;
+  }
+  if (n_steps > 1) {
+    // kernel-per-operator: one step after another from the host
+    const int B = g->bg.cfg.batch;
+    for (int i = 0; i < n_steps; ++i) {
+      mpk_status st = mpk_decode_steps(
+          g, i == 0 ? d_tokens : d_next_tokens + (size_t)(i - 1) * B, kv,
+          d_logits, d_next_tokens + (size_t)i * B, 1, cuda_stream);
+      if (st != MPK_OK) return st;
+    }
     return MPK_OK;
   }
   a.epoch = g->epoch;

@@ -189,7 +189,11 @@ struct StepArgs {
   int num_pages;
   float* logits;
   int32_t* next_tokens;
-  uint32_t epoch;               // step number since the last reset, >= 1
+  uint32_t epoch;               // first step's number since the last reset
+  int n_steps;                  // greedy steps run by this launch (>= 1):
+                                // step i embeds the tokens step i - 1 wrote
+                                // to next_tokens + (i - 1) * B and writes its
+                                // own to next_tokens + i * B
   uint64_t timeout_ns;
 };
 

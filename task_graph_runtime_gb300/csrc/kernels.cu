@@ -263,6 +263,19 @@ __device__ __forceinline__ bool aborted(const KernelParams& P) {
   return ld_relaxed(P.graph.abort_flag) != 0u;
 }
 
+__device__ __forceinline__ bool event_done(const KernelParams& P, int e,
+                                           uint32_t epoch) {
+  const uint32_t target = epoch * P.graph.events[e].count;
+  return (int32_t)(ld_relaxed(P.graph.counters + e) - target) >= 0;
+}
+// The same with acquire semantics: what the event's triggers wrote before
+// triggering is visible to the caller afterwards.
+__device__ __forceinline__ bool event_done_acq(const KernelParams& P, int e,
+                                               uint32_t epoch) {
+  const uint32_t target = epoch * P.graph.events[e].count;
+  return (int32_t)(ld_acquire(P.graph.counters + e) - target) >= 0;
+}
+
 // ------------------------------------------------------------ shared memory
 struct Smem {
   uint8_t* ring;
@@ -272,7 +285,8 @@ struct Smem {
   uint64_t* empty;
   volatile int* ctrl; // [0..1] command, [2] bail-out, [3] aborted at entry,
                       // [4] last-chunk flag, [8..10] leader loop state,
-                      // [13] JIT stage barrier phases
+                      // [13] JIT stage barrier phases, [14] the step of
+                      // this launch the worker is in (multi-step loop)
   TaskDesc* desc;     // [0..1] staged descriptors (slot 2: the fan below)
   uint64_t* times;    // trace: [0] looked-for, [1] ready, [2] operands
                       // staged, [3] last page consumed, [4] body done
@@ -645,8 +659,8 @@ __device__ __forceinline__ bool wait_empty(const KernelParams& P,
 // gp % n_pages with phase (gp / n_pages) & 1 -- the order in which the
 // consumers take them.
 __device__ void producer_role(const KernelParams& P, const Smem& S,
-                              const int32_t* list, int n, uint64_t deadline,
-                              int pid) {
+                              const int32_t* list, int n, int steps,
+                              uint64_t deadline, int pid) {
   static_assert(kProducerWarps == 2, "page ownership alternates");
   const int lane = threadIdx.x & 31;
   uint32_t issued[kMaxRingPages];
@@ -656,10 +670,36 @@ __device__ void producer_role(const KernelParams& P, const Smem& S,
   Ring ring{0, 0};
   int64_t gp = 0;
   int turn = 0;            // gp % 2
-  for (int i = 0; i < n; ++i) {
+  // the list is walked once per step of the launch; weight pages of the
+  // next step stream in while this one ends, but cached K/V (whose position
+  // the step before advances) only after that step's end event
+  for (int step = 0, i = 0; step < steps; ++i) {
+    if (i == n) {
+      if (++step == steps) break;
+      i = -1;
+      continue;
+    }
     const TaskDesc t = P.graph.tasks[list[i]];
     Gemv g;
     const int np = ring_pages_of(P, t, &g);
+    if (np > 0 && step > 0 && t.kind == MPK_TASK_ATTN) {
+      int ok = 1;
+      if (lane == 0) {
+        uint32_t spins = 0;
+        while (!event_done_acq(P, P.graph.end, P.step.epoch + step - 1)) {
+          if ((++spins & 255u) == 0u &&
+              (aborted(P) || globaltimer() > deadline)) {
+            if (!aborted(P)) raise_error(P, MPK_ERR_TIMEOUT);
+            ok = 0;
+            break;
+          }
+        }
+      }
+      if (!__shfl_sync(kFull, ok, 0)) {
+        drain_copies(P, S, issued);
+        return;
+      }
+    }
     // batch-1 weight pages: source pointer and length advance linearly
     const bool lin = np > 0 && is_gemv(t.kind) && g.b1;
     const int64_t span = lin ? (int64_t)g.rpp * g.K : 0;
@@ -714,17 +754,27 @@ __device__ void producer_role(const KernelParams& P, const Smem& S,
 enum { X_PLAIN = 0, X_NORM_ADD = 1, X_NORM_EMBED = 2 };
 struct XSrc {
   int mode;
+  const int32_t* tok;     // embedding mode: this step's tokens
   const uint16_t* a;      // plain source, or first addend
   const uint16_t* c;      // second addend
   const uint16_t* gain;
   uint16_t* resid;        // residual output (tile 0 only), else null
 };
 
-__device__ XSrc x_source(const KernelParams& P, const TaskDesc& t) {
+// Tokens step `step` of the launch embeds: the caller's for step 0, else
+// those step - 1 produced.
+__device__ __forceinline__ const int32_t* step_tokens(const KernelParams& P,
+                                                      int step) {
+  return step == 0 ? P.step.tokens
+                   : P.step.next_tokens + (int64_t)(step - 1) * P.dims.B;
+}
+
+__device__ XSrc x_source(const KernelParams& P, const TaskDesc& t,
+                         int step = 0) {
   const Dims& D = P.dims;
   const int l = t.layer;
   const bool res = (t.flags & TASK_F_RESIDUAL) != 0;
-  XSrc x{X_PLAIN, nullptr, nullptr, nullptr, nullptr};
+  XSrc x{X_PLAIN, step_tokens(P, step), nullptr, nullptr, nullptr, nullptr};
   switch (t.kind) {
     case MPK_TASK_QKV:
       x.gain = layer_w(P, l, MPK_W_LN1);
@@ -814,7 +864,7 @@ __device__ __forceinline__ void pre_values(const KernelParams& P,
                                            float (&v)[8]) {
   PreRaw r;
   if (x.mode == X_NORM_EMBED) {
-    int tok = __ldg(P.step.tokens + b);
+    int tok = __ldcg(x.tok + b);
     tok = min(max(tok, 0), P.dims.V - 1);
     r.a = __ldg(reinterpret_cast<const uint4*>(P.w.embed + (int64_t)tok * K +
                                                k));
@@ -857,7 +907,7 @@ __device__ __forceinline__ void widen8(uint4 v, float4& a, float4& b) {
 __device__ void stage_x_b1(const KernelParams& P, const Smem& S,
                            const TaskDesc& t, const Gemv& g) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const XSrc x = x_source(P, t);
+  const XSrc x = x_source(P, t, S.ctrl[14]);
   const int K = g.K, nch = K >> 3;
   uint4* xs = reinterpret_cast<uint4*>(S.xs);
   if (x.mode == X_PLAIN) {
@@ -906,7 +956,7 @@ __device__ void stage_x_b1(const KernelParams& P, const Smem& S,
 // back only the chunks it copied itself.
 __device__ void norm_stats(const KernelParams& P, const Smem& S,
                            const TaskDesc& t, const Gemv& g) {
-  const XSrc x = x_source(P, t);
+  const XSrc x = x_source(P, t, S.ctrl[14]);
   if (x.mode == X_PLAIN) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int B = P.dims.B, K = g.K, nch = K >> 3;
@@ -920,7 +970,7 @@ __device__ void norm_stats(const KernelParams& P, const Smem& S,
       if (b >= B) break;
       const uint16_t* ra;
       if (x.mode == X_NORM_EMBED) {
-        int tok = __ldg(P.step.tokens + b);
+        int tok = __ldcg(x.tok + b);
         tok = min(max(tok, 0), P.dims.V - 1);
         ra = P.w.embed + (int64_t)tok * K;
       } else {
@@ -962,7 +1012,7 @@ __device__ void norm_stats(const KernelParams& P, const Smem& S,
 // b * kPagePitch bytes; columns up to the next multiple of 16 are zeroed.
 __device__ void stage_x_seg(const KernelParams& P, const Smem& S,
                             const TaskDesc& t, const Gemv& g, int s) {
-  const XSrc x = x_source(P, t);
+  const XSrc x = x_source(P, t, S.ctrl[14]);
   const int B = P.dims.B, K = g.K;
   const int c0 = s * kSegCols, cols = min(kSegCols, K - c0);
   const int nch = cols >> 3, nch16 = ((cols + 15) >> 4) << 1;
@@ -2033,7 +2083,8 @@ __device__ void task_argmax(const KernelParams& P, const Smem& S) {
           bi = oi;
         }
       }
-      P.step.next_tokens[b] = (bi == 0x7fffffff) ? 0 : bi;
+      P.step.next_tokens[(int64_t)S.ctrl[14] * D.B + b] =
+          (bi == 0x7fffffff) ? 0 : bi;
       if (D.chain_ffn == 0)
         P.step.seq_lens[b] = __ldcg(P.step.seq_lens + b) + 1;
     }
@@ -2099,9 +2150,9 @@ __device__ __forceinline__ bool ring_try_pop(RingHdr* hdr, uint64_t* slots,
 // tasks, and runs its empty tasks inline (they only trigger their own
 // event, whose descriptor is read from the graph).
 __device__ void trigger(const KernelParams& P, int e, const EventDesc& ed0,
-                        const int32_t* fan, uint64_t deadline) {
+                        const int32_t* fan, uint32_t epoch,
+                        uint64_t deadline) {
   const DevGraph& G = P.graph;
-  const uint32_t epoch = P.step.epoch;
   if (ed0.flags & EV_FAN_CACHED) {
     bool fire = ed0.count == 1;
     if (!fire) fire = atom_acq_rel_add(G.counters + e, 1u) + 1u == epoch * ed0.count;
@@ -2146,10 +2197,6 @@ __device__ void trigger(const KernelParams& P, int e, const EventDesc& ed0,
   }
 }
 
-__device__ __forceinline__ bool event_done(const KernelParams& P, int e) {
-  const uint32_t target = P.step.epoch * P.graph.events[e].count;
-  return (int32_t)(ld_relaxed(P.graph.counters + e) - target) >= 0;
-}
 
 // ------------------------------------------------------------ roles
 // Asynchronous fetch of one AOT record into shared memory (thread 0).
@@ -2173,11 +2220,15 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
   volatile int* ai_s = S.ctrl + 8;        // queue position of the head record
   volatile int* a1_s = S.ctrl + 9;        // end of this worker's AOT queue
   volatile int* jit_s = S.ctrl + 10;      // JIT ring head
+  volatile int* a0_s = S.ctrl + 11;       // queue start (each step walks it)
+  volatile int* step_s = S.ctrl + 14;     // step of the launch
   if (tid == 0) {
     const int a0 = G.aot_off[w], a1 = G.aot_off[w + 1];
     *jit_s = (int)ld_relaxed(&G.jit_hdr[w].head);
     *ai_s = a0;
     *a1_s = a1;
+    *a0_s = a0;
+    *step_s = 0;
     if (a0 < a1) fetch_rec(G.aot_rec + a0, &S.head[a0 & 1]);
   }
   Ring ring{0, 0};
@@ -2186,7 +2237,8 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
     const int slot = iter & 1;
     if (tid == 0) {
       if (G.trace) S.times[0] = globaltimer();
-      const int ai = *ai_s;
+      const int ai = *ai_s, step = *step_s;
+      const uint32_t epoch = P.step.epoch + (uint32_t)step;
       const bool have_head = ai < *a1_s;
       cp_async_wait_all();
       const AotRec* hr = &S.head[ai & 1];
@@ -2195,10 +2247,16 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
       if (have_head) {
         prefetch_gain(P, hr->desc);   // warm L2 with the prologue's gain
         dep = hr->desc.dep;
-        target = P.step.epoch * hr->dep_count;
+        target = epoch * hr->dep_count;
+        if (dep == G.root && step > 0) {
+          // the step before must have produced this step's tokens and
+          // advanced the sequence lengths
+          dep = G.end;
+          target = (epoch - 1u) * G.events[G.end].count;
+        }
       } else {
         dep = G.end;
-        target = P.step.epoch * G.events[G.end].count;
+        target = epoch * G.events[G.end].count;
       }
       RingHdr* jh = G.jit_hdr + w;
       uint64_t* js = G.jit_slots + (size_t)w * G.jit_cap;
@@ -2227,6 +2285,13 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
             *ai_s = ai + 1;
             if (ai + 1 < *a1_s)
               fetch_rec(G.aot_rec + ai + 1, &S.head[(ai + 1) & 1]);
+          } else if (step + 1 < P.step.n_steps) {
+            // this step has ended: the next one of the launch begins
+            const int a0 = *a0_s;
+            *step_s = step + 1;
+            *ai_s = a0;
+            if (a0 < *a1_s) fetch_rec(G.aot_rec + a0, &S.head[a0 & 1]);
+            cmd = -2;
           }
           break;
         }
@@ -2250,6 +2315,7 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
     consumer_sync();
     const int cmd = S.ctrl[slot];
     ++iter;
+    if (cmd == -2) continue;
     if (cmd < 0) break;
     run_task(P, S, S.desc[slot], ring, deadline);
     consumer_sync();
@@ -2260,7 +2326,17 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
       // the red.release / atom.acq_rel of the trigger is cumulative: it
       // orders every write of the CTA that the barrier above ordered before
       // this thread
-      trigger(P, S.desc[slot].trig, S.tev[slot], S.fan + 2 * slot, deadline);
+      // a JIT task fires in the step its event fired in (a worker can
+      // take one of the next step before it notices this step's end):
+      // the dependent event's counter says which; AOT tasks are in the
+      // worker's current step
+      const TaskDesc& td = S.desc[slot];
+      uint32_t epoch = P.step.epoch + (uint32_t)*step_s;
+      if (td.launch == MPK_LAUNCH_JIT) {
+        const uint32_t c = G.events[td.dep].count;
+        if (c > 0) epoch = ld_relaxed(G.counters + td.dep) / c;
+      }
+      trigger(P, td.trig, S.tev[slot], S.fan + 2 * slot, epoch, deadline);
       if (G.trace) {
         // (task | worker << 32), looked-for, ready, staged, pages done,
         // body done, triggered
@@ -2301,7 +2377,9 @@ __device__ void scheduler_role(const KernelParams& P, int s,
         spins = 0;
       } else {
         ++spins;
-        if (event_done(P, G.end) || aborted(P)) stop = 1;
+        if (event_done(P, G.end, P.step.epoch + P.step.n_steps - 1) ||
+            aborted(P))
+          stop = 1;
         if (spins > 32) __nanosleep(spins > 4096 ? 256 : 32);
         if ((spins & 63u) == 0u && globaltimer() > deadline) {
           raise_error(P, MPK_ERR_TIMEOUT);
@@ -2348,6 +2426,7 @@ __device__ __forceinline__ bool setup_smem(const KernelParams& P, uint8_t* raw,
     mbar_init(&S.jit_bar[0], 1);
     mbar_init(&S.jit_bar[1], 1);
     S.ctrl[13] = 0;   // JIT stage barrier phases
+    S.ctrl[14] = 0;   // step of the launch
     fence_proxy_async_smem();
   }
   __syncthreads();
@@ -2374,8 +2453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<kProducerRegs>();
     if (warp >= kConsumerWarps + kProducerWarps) return;
     const int a0 = P.graph.aot_off[w], a1 = P.graph.aot_off[w + 1];
-    producer_role(P, S, P.graph.aot_list + a0, a1 - a0, deadline,
-                  warp - kConsumerWarps);
+    producer_role(P, S, P.graph.aot_list + a0, a1 - a0, P.step.n_steps,
+                  deadline, warp - kConsumerWarps);
   } else {
     regs_inc<kConsumerRegs>();
     worker_consumers(P, S, w, deadline);
@@ -2395,8 +2474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kConsumerWarps) {
     regs_dec<kProducerRegs>();
     if (warp >= kConsumerWarps + kProducerWarps) return;
-    producer_role(P, S, P.graph.op_tasks + first + blockIdx.x, 1, deadline,
-                  warp - kConsumerWarps);
+    producer_role(P, S, P.graph.op_tasks + first + blockIdx.x, 1, 1,
+                  deadline, warp - kConsumerWarps);
   } else {
     regs_inc<kConsumerRegs>();
     Ring ring{0, 0};

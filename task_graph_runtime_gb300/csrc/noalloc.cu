@@ -196,6 +196,7 @@ extern "C" mpk_status mpk_decode_step_noalloc(
   a.logits = d_logits;
   a.next_tokens = d_next_tokens;
   a.timeout_ns = g->timeout_ns;
+  a.n_steps = 1;
   if (!chain) {
     a.k_pool = static_cast<uint16_t*>(kv->k_pool);
     a.v_pool = static_cast<uint16_t*>(kv->v_pool);

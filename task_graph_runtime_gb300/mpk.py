@@ -118,6 +118,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mpk_bind_weights": ([vp, ctypes.POINTER(_Weights)], st),
         "mpk_decode_step": ([vp, vp, ctypes.POINTER(_KVCache), vp, vp, vp],
                             st),
+        "mpk_decode_steps": ([vp, vp, ctypes.POINTER(_KVCache), vp, vp, i,
+                              vp], st),
         "mpk_get_status": ([vp], st),
         "mpk_set_mode": ([vp, i], st),
         "mpk_export_tgraph": ([vp, ctypes.POINTER(GraphExport)], st),
@@ -289,6 +291,25 @@ class Graph:
             self.handle, tokens.data_ptr(),
             ctypes.byref(kvs) if kvs is not None else None,
             logits.data_ptr(), next_tokens.data_ptr(), s), "mpk_decode_step")
+
+    def decode_steps(self, tokens, kv: Optional[KVCache], logits,
+                     next_tokens, n_steps: int, stream=None):
+        """Enqueue ``n_steps`` greedy steps in one launch (megakernel mode);
+        ``next_tokens`` is int32 [n_steps, batch], ``logits`` receives the
+        last step's."""
+        import torch
+        if stream is None:
+            s = torch.cuda.current_stream().cuda_stream
+        elif isinstance(stream, int):
+            s = stream
+        else:
+            s = stream.cuda_stream
+        kvs = kv.c_struct() if kv is not None else None
+        _check(load_library().mpk_decode_steps(
+            self.handle, tokens.data_ptr(),
+            ctypes.byref(kvs) if kvs is not None else None,
+            logits.data_ptr(), next_tokens.data_ptr(), n_steps, s),
+            "mpk_decode_steps")
 
     def status(self) -> int:
         return load_library().mpk_get_status(self.handle)

@@ -226,3 +226,55 @@ def test_chain_full_size(name):
     gpu, _ = run_gpu(wl, dev_weights(W, wl.shape), None, tok)
     ref, _ = run_oracle(wl, W, None, tok)
     check_steps(gpu, ref)
+
+
+# ---------------------------------------------------- several steps a launch
+def _steps_both_ways(wl, W_host, kv_host, tok, n, **kw):
+    """n greedy steps as n launches and as one launch (mpk_decode_steps),
+    from the same inputs; returns both (tokens [n][B], last logits, K, V,
+    seq_lens)."""
+    shape = wl.shape
+    Wd = dev_weights(W_host, shape)
+    out = []
+    for one_launch in (False, True):
+        g = _graph(wl, **kw)
+        g.bind(Wd)
+        kv = dev_kv(kv_host) if kv_host is not None else None
+        t = torch.from_numpy(np.asarray(tok, np.int32)).cuda()
+        logits = torch.empty(wl.batch, shape.vocab, device="cuda")
+        nxt = torch.empty(n, wl.batch, dtype=torch.int32, device="cuda")
+        if one_launch:
+            g.decode_steps(t, kv, logits, nxt, n)
+        else:
+            for i in range(n):
+                g.decode_step(t if i == 0 else nxt[i - 1], kv, logits, nxt[i])
+        torch.cuda.synchronize()
+        assert g.status() == mpk.MPK_OK, mpk.STATUS_NAMES[g.status()]
+        out.append((nxt.cpu().numpy(), logits.cpu().numpy(),
+                    None if kv is None else (kv.k_pool.clone(), kv.v_pool.clone(),
+                                             kv.seq_lens.cpu().numpy())))
+        g.close()
+    return out
+
+
+@pytest.mark.parametrize("case", ["tiny", "tiny_b3_jit", "chain_b4"])
+def test_several_steps_in_one_launch_equal_step_by_step(case):
+    """Figure 1 of the MPK summary: the decode loop inside one launch.  Step
+    i + 1 embeds step i's tokens and waits for its end; the result must be
+    bit-identical to one launch per step."""
+    base = synth.WORKLOADS["tiny"]
+    if case == "tiny":
+        wl = base
+    elif case == "tiny_b3_jit":
+        wl = dataclasses.replace(base, name="tiny_b3", batch=3,
+                                 ctx=(5, 37, 120), steps=4)
+    else:
+        shape = synth.ModelShape(0, 256, 1, 1, 32, 0, 1024, chain_ffn=512)
+        wl = synth.Workload("chain_small", shape, 4, (), 64, 1)
+    W, kv, tok = _inputs(wl, seed=9)
+    (t1, l1, kv1), (tn, ln, kvn) = _steps_both_ways(wl, W, kv, tok, 4)
+    assert np.array_equal(t1, tn)
+    assert np.array_equal(l1, ln)
+    if kv1 is not None:
+        assert torch.equal(kv1[0], kvn[0]) and torch.equal(kv1[1], kvn[1])
+        assert np.array_equal(kv1[2], kvn[2])
