@@ -1,8 +1,10 @@
-"""Decode benchmark: ms/token and achieved HBM bandwidth of one greedy
-decode step run as one persistent mega-kernel launch.
+"""Decode benchmark: ms/token and achieved HBM bandwidth of greedy decode
+steps run by the persistent mega-kernel (by default 32 steps a launch: the
+decode loop inside one launch; `--steps-per-launch 1` for a launch a step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload qwen3_8b] [--mode mega|kpo|kpo_graph]
+                  [--steps-per-launch S]
 
 A step is one pass of the whole decode path (every operator of every layer,
 lm_head and argmax) for one batch.  Inputs are synthetic and seeded (random
@@ -271,7 +273,13 @@ def run_ours(args, rank, world, local_rank):
     logits = torch.empty(B, s.vocab, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     ex = g.export()
-    n_launch_per_step = 1 if mode == mpk.MODE_MEGAKERNEL else ex["n_ops"]
+    # megakernel: several steps a launch (the decode loop inside the kernel);
+    # a launch never crosses a rewind of the sequence lengths
+    spl = max(1, min(args.steps_per_launch, block)) \
+        if mode == mpk.MODE_MEGAKERNEL else 1
+    while block % spl:
+        spl -= 1
+    nxt_buf = torch.empty(spl, B, dtype=torch.int32, device=dev)
 
     def rewind(i):
         if kv is not None and i % block == 0:
@@ -286,6 +294,11 @@ def run_ours(args, rank, world, local_rank):
         else:
             g.decode_step(toks[i % 2], kv, logits, toks[(i + 1) % 2], stream)
 
+    def launch_block(i):
+        """Steps [i, i + spl) in one megakernel launch."""
+        g.decode_steps(toks[0], kv, logits, nxt_buf, spl, stream)
+        toks[0].copy_(nxt_buf[spl - 1], non_blocking=True)
+
     def step(i):
         rewind(i)
         launch(i, mode)
@@ -293,13 +306,17 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i)
+        if spl > 1:
+            rewind(0)
+            launch_block(0)
         torch.cuda.synchronize(dev)
         st = g.status()
         if st != mpk.MPK_OK:
             raise RuntimeError(f"warm-up failed: {mpk.STATUS_NAMES[st]}")
-        # per-launch events (megakernel: one launch per step)
+        # per-launch events
+        starts = list(range(0, args.steps, spl))
         ev = [(torch.cuda.Event(enable_timing=True),
-               torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+               torch.cuda.Event(enable_timing=True)) for _ in starts]
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         if world > 1:
@@ -309,11 +326,15 @@ def run_ours(args, rank, world, local_rank):
         clocks.start()
         time.sleep(0.3)
         start.record(stream)
-        for i in range(args.steps):
+        for j, i in enumerate(starts):
             rewind(i)
-            ev[i][0].record(stream)
-            launch(i, mode)
-            ev[i][1].record(stream)
+            ev[j][0].record(stream)
+            if spl > 1 and i + spl <= args.steps:
+                launch_block(i)
+            else:
+                for k in range(i, min(i + spl, args.steps)):
+                    launch(k, mode)
+            ev[j][1].record(stream)
         end.record(stream)
         torch.cuda.synchronize(dev)
         clk = clocks.stop()
@@ -389,7 +410,8 @@ def run_ours(args, rank, world, local_rank):
     ms_step = total_ms / args.steps
     launch_avg = statistics.mean(launch_ms)
     peak, peak_kind = measured_peaks()
-    achieved = bytes_step / (launch_avg * 1e-3) / 1e9
+    # one launch = spl whole steps
+    achieved = spl * bytes_step / (launch_avg * 1e-3) / 1e9
     traffic = load_traffic(args.workload, args.mode)
     out = {
         "metric": METRIC,
@@ -428,7 +450,9 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_ms / B, 5), "unit": "ms/token",
                 "h2d_bytes_per_step": 4 * B, "d2h_bytes_per_step": 4 * B,
                 "steps": e2e_steps},
-        "gpu_launches": args.steps * n_launch_per_step,
+        "gpu_launches": len(starts) if mode == mpk.MODE_MEGAKERNEL
+                        else args.steps * ex["n_ops"],
+        "steps_per_launch": spl,
         "same_run_modes": compare,
         "graph": {"tasks": ex["n_tasks"], "events": ex["n_events"],
                   "empty_tasks": ex["n_empty"], "workers": ex["n_workers"],
@@ -499,6 +523,9 @@ def main():
     ap.add_argument("--mode", default="mega",
                     choices=["mega", "kpo", "kpo_graph"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--steps-per-launch", type=int, default=32,
+                    help="megakernel: greedy steps per launch (the decode "
+                         "loop inside one launch); 1: a launch per step")
     ap.add_argument("--no-compare", dest="compare", action="store_false",
                     help="skip the same-run kernel-per-operator timings")
     args = ap.parse_args()
