@@ -1010,36 +1010,69 @@ __device__ void norm_stats(const KernelParams& P, const Smem& S,
 
 // Batch > 1: stage column segment s of every sequence into S.xs, row b at
 // b * kPagePitch bytes; columns up to the next multiple of 16 are zeroed.
+// Norm modes: the segment goes in quarters of 512 columns.  Each quarter's
+// raw words arrive by asynchronous copies -- the first addend (or the
+// embedding row) straight into its place in the row, the second addend
+// into a scratch area after the rows -- and are then normalised in place.
+constexpr int kSegQuarter = 64;   // chunks (of 8 columns)
 __device__ void stage_x_seg(const KernelParams& P, const Smem& S,
                             const TaskDesc& t, const Gemv& g, int s) {
   const XSrc x = x_source(P, t, S.ctrl[14]);
   const int B = P.dims.B, K = g.K;
   const int c0 = s * kSegCols, cols = min(kSegCols, K - c0);
   const int nch = cols >> 3, nch16 = ((cols + 15) >> 4) << 1;
+  auto row = [&](int b) {
+    return reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(S.xs) +
+                                    (size_t)b * kPagePitch);
+  };
   consumer_sync();   // every warp is done with the previous segment
-  for (int idx = threadIdx.x; idx < B * nch16; idx += kConsumers) {
-    const int b = idx / nch16, ch = idx - b * nch16;
-    uint4* dst = reinterpret_cast<uint4*>(
-        reinterpret_cast<uint8_t*>(S.xs) + (size_t)b * kPagePitch) + ch;
-    if (ch >= nch) {
-      *dst = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    const int k = c0 + ch * 8;
-    if (x.mode == X_PLAIN) {
-      cp_async16(dst, x.a + (int64_t)b * K + k);   // all in flight together
-    } else {
-      float v[8];
-      pre_values(P, x, b, K, k, v);
-      *dst = norm8(v, S.scratch[32 + b],
-                   __ldg(reinterpret_cast<const uint4*>(x.gain + k)));
-    }
+  // columns past the segment up to the next multiple of 16: zero
+  for (int idx = threadIdx.x; idx < B * (nch16 - nch); idx += kConsumers) {
+    const int b = idx / (nch16 - nch), ch = nch + idx % (nch16 - nch);
+    row(b)[ch] = make_uint4(0, 0, 0, 0);
   }
   if (x.mode == X_PLAIN) {
+    for (int idx = threadIdx.x; idx < B * nch; idx += kConsumers) {
+      const int b = idx / nch, ch = idx - b * nch;
+      cp_async16(row(b) + ch, x.a + (int64_t)b * K + c0 + ch * 8);
+    }
     cp_async_commit();
     cp_async_wait_all();
+    consumer_sync();
+    return;
   }
-  consumer_sync();
+  uint4* tmp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(S.xs) +
+                                        (size_t)B * kPagePitch);   // [B][64]
+  const bool embed = x.mode == X_NORM_EMBED;
+  for (int q0 = 0; q0 < nch; q0 += kSegQuarter) {
+    const int nq = min(kSegQuarter, nch - q0);
+    for (int idx = threadIdx.x; idx < B * nq; idx += kConsumers) {
+      const int b = idx / nq, ch = q0 + idx % nq;
+      const int64_t k = c0 + ch * 8;
+      if (embed) {
+        int tok = __ldcg(x.tok + b);
+        tok = min(max(tok, 0), P.dims.V - 1);
+        cp_async16(row(b) + ch, P.w.embed + (int64_t)tok * K + k);
+      } else {
+        cp_async16(row(b) + ch, x.a + (int64_t)b * K + k);
+        cp_async16(tmp + b * kSegQuarter + (ch - q0), x.c + (int64_t)b * K + k);
+      }
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    consumer_sync();
+    for (int idx = threadIdx.x; idx < B * nq; idx += kConsumers) {
+      const int b = idx / nq, ch = q0 + idx % nq;
+      PreRaw raw;
+      raw.a = row(b)[ch];
+      raw.c = embed ? make_uint4(0, 0, 0, 0) : tmp[b * kSegQuarter + (ch - q0)];
+      float v[8];
+      pre_finish(x, raw, v);
+      row(b)[ch] = norm8(v, S.scratch[32 + b],
+                         __ldg(reinterpret_cast<const uint4*>(x.gain + c0) + ch));
+    }
+    consumer_sync();   // the scratch area is reused by the next quarter
+  }
 }
 
 // ------------------------------------------------------------ epilogue

@@ -19,7 +19,9 @@ bool smem_layout(const BuiltGraph& bg, int pages_req, int limit,
   const int kmax = chain ? std::max(s.hidden, s.chain_ffn)
                          : std::max({s.hidden, s.n_q_heads * s.head_dim,
                                      s.ffn});
-  int xs = B == 1 ? round_up(kmax * 2, 16) : B * kPagePitch;   // bf16 x at B=1
+  // bf16 x at batch 1; at batch > 1 one 2048-column segment of every
+  // sequence plus a 512-column scratch row per sequence for the staging
+  int xs = B == 1 ? round_up(kmax * 2, 16) : B * kPagePitch + B * 64 * 16;
   if (!chain) {
     const int grp = s.n_q_heads / s.n_kv_heads, d = s.head_dim;
     // query rows + 8 warp records (+ the new K/V rows)
