@@ -412,7 +412,7 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     # one launch = spl whole steps
     achieved = spl * bytes_step / (launch_avg * 1e-3) / 1e9
-    traffic = load_traffic(args.workload, args.mode)
+    traffic = load_traffic(args.workload, args.mode, spl)
     out = {
         "metric": METRIC,
         "value": round(total_ms / (args.steps * B * world), 5),
@@ -461,10 +461,12 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
-def load_traffic(workload, mode):
+def load_traffic(workload, mode, steps_per_launch=1):
     """DRAM bytes per launch from the committed ncu summary
     profiles/traffic_<workload>_<mode>.txt ("key: value" lines), if it was
-    taken on the current kernel source (else null)."""
+    taken on the current kernel source (else null).  The summary holds the
+    bytes of a one-step launch; a launch of S steps moves S times as many
+    (every step streams the same weights and cache)."""
     import hashlib
     p = os.path.join(ROOT, "profiles", f"traffic_{workload}_{mode}.txt")
     src = os.path.join(ROOT, "task_graph_runtime_gb300", "csrc", "kernels.cu")
@@ -477,9 +479,9 @@ def load_traffic(workload, mode):
                 k, v = line.split(":", 1)
                 d[k.strip()] = v.strip()
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if d.get("kernels_sha") != h or "dram_bytes_per_launch" not in d:
+    if d.get("kernels_sha") != h or "dram_bytes_per_step" not in d:
         return None
-    return int(float(d["dram_bytes_per_launch"]))
+    return int(float(d["dram_bytes_per_step"])) * steps_per_launch
 
 
 def run_reference(args):
