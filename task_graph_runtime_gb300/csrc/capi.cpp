@@ -313,6 +313,7 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
   CK(g->d_status.alloc(2));
   CK(g->d_merge_cnt.alloc((size_t)merge_counters(g->bg)));
   CK(g->d_jit_hdr.alloc(W));
+  CK(g->d_jit_cost.alloc(1));
   CK(g->d_sched_hdr.alloc(S));
   CK(g->d_jit_slots.alloc((size_t)W * kJitCap));
   CK(g->d_sched_slots.alloc((size_t)S * kSchedCap));
@@ -359,6 +360,7 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
   G.counters = g->d_counters.p;
   G.merge_cnt = g->d_merge_cnt.p;
   G.jit_hdr = g->d_jit_hdr.p;
+  G.jit_cost = g->d_jit_cost.p;
   G.jit_slots = g->d_jit_slots.p;
   G.sched_hdr = g->d_sched_hdr.p;
   G.sched_slots = g->d_sched_slots.p;
@@ -390,6 +392,7 @@ mpk_status mpk_reset(mpk_graph* g) {
   CK(cudaMemset(g->d_status.p, 0, g->d_status.n * sizeof(uint32_t)));
   CK(cudaMemset(g->d_merge_cnt.p, 0, g->d_merge_cnt.n * sizeof(uint32_t)));
   CK(cudaMemset(g->d_jit_hdr.p, 0, g->d_jit_hdr.n * sizeof(RingHdr)));
+  CK(cudaMemset(g->d_jit_cost.p, 0, sizeof(unsigned long long)));
   CK(cudaMemset(g->d_sched_hdr.p, 0, g->d_sched_hdr.n * sizeof(RingHdr)));
   CK(cudaMemset(g->d_jit_slots.p, 0, g->d_jit_slots.n * sizeof(uint64_t)));
   CK(cudaMemset(g->d_sched_slots.p, 0, g->d_sched_slots.n * sizeof(uint64_t)));

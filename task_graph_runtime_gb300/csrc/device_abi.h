@@ -156,6 +156,8 @@ struct DevGraph {
   uint32_t* counters;          // [n_events]
   uint32_t* merge_cnt;         // [L][B][Hkv] attention chunk arrivals
   RingHdr* jit_hdr;            // [W]
+  unsigned long long* jit_cost;  // JIT work dealt so far (tokens + fixed
+                                 // part per task), over all steps
   uint64_t* jit_slots;         // [W][jit_cap]
   RingHdr* sched_hdr;          // [S]
   uint64_t* sched_slots;       // [S][sched_cap]

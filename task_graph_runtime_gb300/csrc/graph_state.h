@@ -63,6 +63,7 @@ struct mpk_graph {
   DevBuf<int32_t> d_aot, d_aot_off, d_op_tasks;
   DevBuf<mpk::AotRec> d_aot_rec;
   DevBuf<uint32_t> d_counters, d_status, d_merge_cnt;
+  DevBuf<unsigned long long> d_jit_cost;
   DevBuf<mpk::RingHdr> d_jit_hdr, d_sched_hdr;
   DevBuf<uint64_t> d_jit_slots, d_sched_slots;
   DevBuf<char> d_act;

@@ -2399,6 +2399,23 @@ __device__ void scheduler_role(const KernelParams& P, int s,
   uint64_t* slots = G.sched_slots + (size_t)s * G.sched_cap;
   uint32_t head = (lane == 0) ? ld_relaxed(&hdr->head) : 0;
   uint32_t cursor = (uint32_t)(((int64_t)s * G.W) / G.S);
+  // JIT attention chunks differ in length as the sequences do: they are
+  // dealt by cost, each worker receiving a run of about `quantum` of the
+  // work of one layer (the tokens of all chunks plus a fixed part per task,
+  // over the workers), in the order a global cost counter hands out
+  constexpr uint32_t kJitFixedCost = 64;
+  unsigned long long quantum = 0;
+  if (G.jit_cost && P.step.seq_lens && P.dims.chain_ffn == 0) {   // decoder
+    uint64_t tok = 0;
+    for (int b = lane; b < P.dims.B; b += 32)
+      tok += (uint64_t)max(__ldcg(P.step.seq_lens + b) + 1, 0);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tok += __shfl_xor_sync(kFull, tok, o);
+    const uint64_t per_layer =
+        tok * (uint64_t)P.dims.Hkv +
+        (uint64_t)kJitFixedCost * P.dims.B * P.dims.Hkv * P.dims.C;
+    quantum = max(per_layer / (uint64_t)G.W, (uint64_t)1);
+  }
   uint32_t spins = 0;
   while (true) {
     int e = -1, stop = 0;
@@ -2428,8 +2445,18 @@ __device__ void scheduler_role(const KernelParams& P, int s,
     const int n = ed.last - ed.first + 1;
     for (int i = lane; i < n; i += 32) {
       const int t = ed.first + i;
-      if (G.tasks[t].launch != MPK_LAUNCH_JIT) continue;
-      const int w = (int)((cursor + (uint32_t)i) % (uint32_t)G.W);
+      const TaskDesc td = G.tasks[t];
+      if (td.launch != MPK_LAUNCH_JIT) continue;
+      int w = (int)((cursor + (uint32_t)i) % (uint32_t)G.W);
+      if (quantum > 0 && td.kind == MPK_TASK_ATTN) {
+        const int pos = __ldcg(P.step.seq_lens + td.b);
+        int t0 = 0, t1 = 0;
+        if (pos >= 0) chunk_range(td.c, pos + 1, P.dims.C, t0, t1);
+        const unsigned long long cost =
+            kJitFixedCost + (unsigned long long)max(t1 - t0, 0);
+        const unsigned long long at = atomicAdd(G.jit_cost, cost);
+        w = (int)(((at + cost / 2) / quantum) % (unsigned long long)G.W);
+      }
       ring_push(P, G.jit_hdr + w, G.jit_slots + (size_t)w * G.jit_cap,
                 G.jit_cap, (uint32_t)t, deadline);
     }

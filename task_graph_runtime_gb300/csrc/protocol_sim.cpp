@@ -7,6 +7,8 @@
 // the kernel's worker_consumers / scheduler_role / trigger take (MPK: A
 // Compiler and Runtime for Mega-Kernelizing Tensor Programs, §2 Q2 runtime
 // and Figure 8, AOT vs JIT).  Task bodies are replaced by random delays.
+// Which worker a JIT task goes to does not change the protocol; the model
+// deals JIT tasks round-robin (the kernel deals attention chunks by cost).
 //
 // Checked for every executed task: it runs exactly once per step, and every
 // task that triggers the event it waits on has finished in the same step
