@@ -370,6 +370,9 @@ mpk_status mpk_bind_weights(mpk_graph* g, const mpk_weights* w) {
   G.abort_flag = g->d_status.p + 1;
   G.W = W;
   G.S = S;
+  G.has_jit = 0;
+  for (const TaskDesc& t : g->h_tasks)
+    if (t.launch == MPK_LAUNCH_JIT) G.has_jit = 1;
   G.sched_warps_per_sm = g->sched_warps_per_sm;
   P.w.embed = static_cast<const uint16_t*>(w->embed);
   P.w.final_norm = static_cast<const uint16_t*>(w->final_norm);

@@ -168,6 +168,8 @@ struct DevGraph {
   uint32_t* trace_count;
   uint32_t trace_cap;          // records
   int W;                       // worker CTAs
+  int has_jit;                 // any JIT task (else workers never poll
+                               // their JIT rings)
   int S;                       // scheduler warps in total
   int sched_warps_per_sm;
 };

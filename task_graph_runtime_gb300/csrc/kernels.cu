@@ -2298,7 +2298,7 @@ __device__ void worker_consumers(const KernelParams& P, const Smem& S, int w,
       uint32_t spins = 0;
       while (!S.ctrl[2]) {
         uint32_t v;
-        if (ring_try_pop(jh, js, G.jit_cap, jit_head, v)) {
+        if (G.has_jit && ring_try_pop(jh, js, G.jit_cap, jit_head, v)) {
           cmd = (int)v;
           S.desc[slot] = G.tasks[cmd];
           S.tev[slot] = G.events[S.desc[slot].trig];
