@@ -1,6 +1,6 @@
 """Decode benchmark: ms/token and achieved HBM bandwidth of greedy decode
-steps run by the persistent mega-kernel (by default 32 steps a launch: the
-decode loop inside one launch; `--steps-per-launch 1` for a launch a step).
+steps run by the persistent mega-kernel (at batch 1 by default 32 steps a
+launch: the decode loop inside one launch; `--steps-per-launch S` to set).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload qwen3_8b] [--mode mega|kpo|kpo_graph]
@@ -275,8 +275,8 @@ def run_ours(args, rank, world, local_rank):
     ex = g.export()
     # megakernel: several steps a launch (the decode loop inside the kernel);
     # a launch never crosses a rewind of the sequence lengths
-    spl = max(1, min(args.steps_per_launch, block)) \
-        if mode == mpk.MODE_MEGAKERNEL else 1
+    want = args.steps_per_launch or (32 if B == 1 else 1)
+    spl = max(1, min(want, block)) if mode == mpk.MODE_MEGAKERNEL else 1
     while block % spl:
         spl -= 1
     nxt_buf = torch.empty(spl, B, dtype=torch.int32, device=dev)
@@ -525,9 +525,10 @@ def main():
     ap.add_argument("--mode", default="mega",
                     choices=["mega", "kpo", "kpo_graph"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--steps-per-launch", type=int, default=32,
+    ap.add_argument("--steps-per-launch", type=int, default=0,
                     help="megakernel: greedy steps per launch (the decode "
-                         "loop inside one launch); 1: a launch per step")
+                         "loop inside one launch); 1: a launch per step; "
+                         "0: 32 at batch 1, 1 above (measured faster)")
     ap.add_argument("--no-compare", dest="compare", action="store_false",
                     help="skip the same-run kernel-per-operator timings")
     args = ap.parse_args()
