@@ -1405,58 +1405,65 @@ __device__ void gemv_cc(const KernelParams& P, const Smem& S,
 }
 
 // Batch >= 8 on tensor cores: mma.sync m16n8k16 with the sequences as M
-// (rows >= batch repeat the last sequence and are discarded) and the page's
-// 8 weight rows as N.  Column segments outer; warp w owns row groups
-// j = w and j = w + 8 (at most 16 groups per tile), so no cross-warp
-// reduction is needed.
+// (rows >= batch repeat the last sequence and are discarded) and a page's 8
+// weight rows as N.  Column segments outer.  Every warp takes its own
+// 256 columns (16 k-steps) of every page, so all 8 warps consume each page
+// together and the ring drains as fast as it fills.  At the end the 8
+// per-warp partial sums of every output are added in warp order.
 __device__ void gemv_mma(const KernelParams& P, const Smem& S,
                          const TaskDesc& t, const Gemv& g, Ring& ring,
                          uint64_t deadline) {
   constexpr int kMaxGroups = 16;
+  constexpr int kKS = kSegCols / 16 / kConsumerWarps;   // k-steps a warp
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int B = P.dims.B, RP = g.ngroups * kPageRows;
   norm_stats(P, S, t, g);
   stamp(P, S, 2);
-  float acc[2][2][4];
+  float acc[kMaxGroups][4];
 #pragma unroll
-  for (int a = 0; a < 2; ++a)
+  for (int j = 0; j < kMaxGroups; ++j)
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[a][c][e] = 0.f;
+    for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
   // ldmatrix row addresses: A = x rows (sequences), B = page rows
   const int arow = min((lane & 7) + ((lane >> 3) & 1) * 8, B - 1);
   const uint32_t a_base = smem_addr(S.xs) + arow * kPagePitch +
-                          ((lane >> 4) * 8) * 2;
-  const uint32_t b_off = (lane & 7) * kPagePitch + ((lane >> 3) * 8) * 2;
+                          ((lane >> 4) * 8) * 2 + warp * kKS * 32;
+  const uint32_t b_off = (lane & 7) * kPagePitch + ((lane >> 3) * 8) * 2 +
+                         warp * kKS * 32;
   const int kq = (lane & 3) * 2;   // this lane's k within an 8-column block
   for (int s = 0; s < g.nsegs; ++s) {
     stage_x_seg(P, S, t, g, s);
     const int cols = min(kSegCols, g.K - s * kSegCols);
-    const int ksteps = (cols + 15) >> 4;
+    const int nks = min(kKS, ((cols + 15) >> 4) - warp * kKS);   // may be <= 0
+    const int kc = cols - warp * kKS * 16;   // columns left from this slice
 #pragma unroll
     for (int j = 0; j < kMaxGroups; ++j) {
       if (j < g.ngroups) {
         const bool have = wait_full(P, S, ring, deadline);
-        if (have && (j & 7) == warp) {
+        if (have && nks > 0) {
           const uint32_t pb = smem_addr(page_ptr(S, ring.slot)) + b_off;
-          float (&c0)[4] = acc[j >> 3][0];
-          float (&c1)[4] = acc[j >> 3][1];
-          for (int ks = 0; ks < ksteps; ks += 2) {
-            uint32_t b0, b1, b2, b3, x0, x1, x2, x3;
-            ldsm_x4(pb + ks * 32, b0, b1, b2, b3);
-            ldsm_x4(a_base + ks * 32, x0, x1, x2, x3);
-            const int kb = ks * 16 + kq;
-            if (kb >= cols) b0 = 0u;
-            if (kb + 8 >= cols) b1 = 0u;
-            mma_16816(c0, x0, x1, x2, x3, b0, b1);
-            if (ks + 1 < ksteps) {
-              ldsm_x4(a_base + ks * 32 + 32, x0, x1, x2, x3);
-              if (kb + 16 >= cols) b2 = 0u;
-              if (kb + 24 >= cols) b3 = 0u;
-              mma_16816(c1, x0, x1, x2, x3, b2, b3);
+          // two chains (even and odd k-steps), joined after the page
+          float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < kKS; kk += 2) {
+            if (kk < nks) {
+              uint32_t b0, b1, b2, b3, x0, x1, x2, x3;
+              ldsm_x4(pb + kk * 32, b0, b1, b2, b3);
+              ldsm_x4(a_base + kk * 32, x0, x1, x2, x3);
+              const int kb = kk * 16 + kq;
+              if (kb >= kc) b0 = 0u;
+              if (kb + 8 >= kc) b1 = 0u;
+              mma_16816(e0, x0, x1, x2, x3, b0, b1);
+              if (kk + 1 < nks) {
+                ldsm_x4(a_base + kk * 32 + 32, x0, x1, x2, x3);
+                if (kb + 16 >= kc) b2 = 0u;
+                if (kb + 24 >= kc) b3 = 0u;
+                mma_16816(e1, x0, x1, x2, x3, b2, b3);
+              }
             }
           }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[j][e] += e0[e] + e1[e];
         }
         release_page(S, ring, have);
       }
@@ -1464,27 +1471,34 @@ __device__ void gemv_mma(const KernelParams& P, const Smem& S,
     skip_extra_groups(P, S, g, kMaxGroups, ring, deadline);
   }
   stamp(P, S, 3);
+  // per-warp partials [warp][B][RP] in the x buffer (8 * B * 128 floats fit
+  // in its B * (kPagePitch + 1024) bytes), once every warp is done with x
+  consumer_sync();
+  float* part = reinterpret_cast<float*>(S.xs);
+  const int BR = B * RP;
   // D fragment: rows (sequences) lane/4 and lane/4 + 8, columns (page rows)
   // (lane % 4) * 2 and + 1
   const int bq = lane >> 2, nq = (lane & 3) * 2;
 #pragma unroll
-  for (int a = 0; a < 2; ++a) {
-    const int j = warp + 8 * a;
+  for (int j = 0; j < kMaxGroups; ++j) {
     if (j < g.ngroups) {
-      const float d0 = acc[a][0][0] + acc[a][1][0];
-      const float d1 = acc[a][0][1] + acc[a][1][1];
-      const float d2 = acc[a][0][2] + acc[a][1][2];
-      const float d3 = acc[a][0][3] + acc[a][1][3];
-      const int pr = j * kPageRows + nq;
+      float* q = part + warp * BR + j * kPageRows + nq;
       if (bq < B) {
-        S.res[bq * RP + pr] = d0;
-        S.res[bq * RP + pr + 1] = d1;
+        q[bq * RP] = acc[j][0];
+        q[bq * RP + 1] = acc[j][1];
       }
       if (bq + 8 < B) {
-        S.res[(bq + 8) * RP + pr] = d2;
-        S.res[(bq + 8) * RP + pr + 1] = d3;
+        q[(bq + 8) * RP] = acc[j][2];
+        q[(bq + 8) * RP + 1] = acc[j][3];
       }
     }
+  }
+  consumer_sync();
+  for (int i = threadIdx.x; i < BR; i += kConsumers) {
+    float v = part[i];
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) v += part[w * BR + i];
+    S.res[i] = v;
   }
   consumer_sync();
   gemv_epilogue(P, S, t, g);
