@@ -1674,7 +1674,7 @@ __device__ __forceinline__ void attn_tokens(
 
 // JIT attention streams its cached tokens through two shared-memory stages
 // of kJitStageTok tokens (K rows then V rows), filled by bulk copies that
-// consumer thread 0 issues, one per run of tokens inside a KV page.
+// one consumer thread issues, one per run of tokens inside a KV page.
 constexpr int kJitStageTok = 64;
 __device__ __host__ __forceinline__ int jit_stage_bytes(int d) {
   return kJitStageTok * d * 2 * 2;   // K and V rows of one stage
@@ -1682,8 +1682,9 @@ __device__ __host__ __forceinline__ int jit_stage_bytes(int d) {
 
 // Copy the cached tokens [a, e) of (layer l, sequence b, KV head g) into a
 // stage (K rows at kdst, V rows at vdst, row 0 = token a); completes on
-// `bar` (thread 0).  Unmapped pages raise MPK_ERR_KV_PAGE and are skipped
-// (their bytes are not expected, so the stage still completes).
+// `bar`.  Called by the issuing thread alone.  Unmapped pages raise
+// MPK_ERR_KV_PAGE and are skipped (their bytes are not expected, so the
+// stage still completes).
 __device__ void issue_kv_stage(const KernelParams& P, int l, int b, int g,
                                int a, int e, uint8_t* kdst, uint8_t* vdst,
                                uint64_t* bar, uint64_t policy) {
@@ -1825,6 +1826,30 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
     t0 = t1 = 0;
   }
   const bool has_new = ok && t1 == n && t1 > t0;
+  // JIT: the cached tokens [t0, ce) stream through two stages; the first two
+  // fills go out before the prologue (they do not depend on it), so their
+  // latency overlaps the query and RoPE work.  They are issued by lane 0 of
+  // the last warp (no query head of its own unless the group has more than
+  // 6 heads), which tracks the fills issued and not yet seen complete (bit
+  // per stage) and the phase each of them completes.
+  const bool issuer = tid == kConsumers - 32;
+  const int ce = has_new ? pos : t1;
+  const int nsub = PRE ? 0 : (t1 - t0 + kJitStageTok - 1) / kJitStageTok;
+  const int sb = jit_stage_bytes(d) / 2;   // K (or V) rows of one stage
+  uint64_t* sbar = S.jit_bar;
+  uint32_t ph = (uint32_t)S.ctrl[13];
+  const uint64_t policy = PRE ? 0ull : evict_first_policy();
+  uint32_t pend = 0, pend_ph = 0;
+  if (!PRE && issuer) {
+    for (int s = 0; s < 2 && s < nsub; ++s) {
+      const int a = t0 + s * kJitStageTok;
+      issue_kv_stage(P, l, b, g, a, min(ce, a + kJitStageTok),
+                     stage0 + s * 2 * sb, stage0 + s * 2 * sb + sb, &sbar[s],
+                     policy);
+      pend |= 1u << s;
+      pend_ph = (pend_ph & ~(1u << s)) | (ph & (1u << s));
+    }
+  }
   // ---- prologue: queries (and the new key/value) into shared memory
   {
     const uint16_t* qkv = lt(P, l, P.act.o_qkv) +
@@ -1891,25 +1916,6 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
   } else {
     // cached tokens [t0, ce) come through the stages; the new token (if
     // this chunk holds it) from knew/vnew
-    const int ce = has_new ? pos : t1;
-    const int nsub = (t1 - t0 + kJitStageTok - 1) / kJitStageTok;
-    const int sb = jit_stage_bytes(d) / 2;   // K (or V) rows of one stage
-    uint64_t* sbar = S.jit_bar;
-    uint32_t ph = (uint32_t)S.ctrl[13];
-    const uint64_t policy = evict_first_policy();
-    // thread 0: fills issued and not yet seen complete (bit per stage), and
-    // the phase each of them completes
-    uint32_t pend = 0, pend_ph = 0;
-    if (tid == 0) {
-      for (int s = 0; s < 2 && s < nsub; ++s) {
-        const int a = t0 + s * kJitStageTok;
-        issue_kv_stage(P, l, b, g, a, min(ce, a + kJitStageTok),
-                       stage0 + s * 2 * sb, stage0 + s * 2 * sb + sb,
-                       &sbar[s], policy);
-        pend |= 1u << s;
-        pend_ph = (pend_ph & ~(1u << s)) | (ph & (1u << s));
-      }
-    }
     for (int s = 0; s < nsub; ++s) {
       const int st = s & 1;
       bool got = !S.ctrl[2];
@@ -1930,7 +1936,7 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
             reinterpret_cast<const uint16_t*>(stage0 + st * 2 * sb + sb), lo,
             lo, hi, has_new ? pos : -1, knew, vnew, m_run, l_run, acc);
       consumer_sync();   // the stage is free again
-      if (tid == 0 && s + 2 < nsub && !S.ctrl[2]) {
+      if (issuer && s + 2 < nsub && !S.ctrl[2]) {
         const int a = lo + 2 * kJitStageTok;
         issue_kv_stage(P, l, b, g, a, min(ce, a + kJitStageTok),
                        stage0 + st * 2 * sb, stage0 + st * 2 * sb + sb,
@@ -1939,7 +1945,7 @@ __device__ void attn_body(const KernelParams& P, const Smem& S,
         pend_ph = (pend_ph & ~(1u << st)) | (ph & (1u << st));
       }
     }
-    if (tid == 0) {
+    if (issuer) {
       // an abandoned fill still completes (its bytes were expected): wait
       // (bounded) so that no copy lands in shared memory after the task
       const uint64_t lim = globaltimer() + 200000000ull;
