@@ -90,7 +90,9 @@ typedef struct {
   int attn_chunks;        /* split-KV chunks per (sequence, KV head).  0:
                              max(1, min(ceil(max_ctx/128),
                              ceil(4W/(batch*n_kv_heads))))                  */
-  int num_sched_sms;      /* SMs running scheduler warps. 0: 4 (Table 1)    */
+  int num_sched_sms;      /* SMs running scheduler warps.  0: 4 (Table 1)
+                             when the graph has JIT tasks, none when every
+                             task is AOT (no dispatch: all SMs are workers) */
   int sched_warps_per_sm; /* 0: 4 (Table 1)                                 */
   int smem_pages;         /* weight pages per worker (batch 1: 32 KB of
                              whole rows; batch > 1: 8 rows x 2048 columns,

@@ -178,6 +178,12 @@ const char* mpk_status_string(mpk_status s) {
   return "unknown status";
 }
 
+static bool has_jit_tasks(const BuiltGraph& bg) {
+  for (int32_t l : bg.launch)
+    if (l == MPK_LAUNCH_JIT) return true;
+  return false;
+}
+
 mpk_status mpk_build_tgraph(const mpk_model_shape* shape,
                             const mpk_tile_sizes* tiles, int batch,
                             mpk_graph** out) {
@@ -185,13 +191,18 @@ mpk_status mpk_build_tgraph(const mpk_model_shape* shape,
   *out = nullptr;
   mpk_tile_sizes t{};
   if (tiles) t = *tiles;
-  int sched_sms = t.num_sched_sms > 0 ? t.num_sched_sms : 4;
+  // Scheduler SMs: as given, else (0) 4 (Table 1) when the graph has JIT
+  // tasks and none when every task is AOT -- such a graph never dispatches,
+  // so every SM becomes a worker.
+  const bool auto_sched = t.num_sched_sms <= 0;
+  int sched_sms = auto_sched ? 0 : t.num_sched_sms;
   int sched_warps = t.sched_warps_per_sm > 0 ? t.sched_warps_per_sm : 4;
   if (sched_warps > 9) return MPK_ERR_INVALID_ARG;
   int W = t.num_workers;
   if (W < 0) return MPK_ERR_INVALID_ARG;
+  int sms = 0;
   if (W == 0) {
-    int dev = 0, sms = 0;
+    int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
             cudaSuccess)
@@ -212,6 +223,16 @@ mpk_status mpk_build_tgraph(const mpk_model_shape* shape,
   std::string err;
   mpk_status st = build_tgraph(cfg, &g->bg, &err);
   if (st != MPK_OK) return st;
+  if (auto_sched && has_jit_tasks(g->bg)) {
+    sched_sms = 4;
+    if (sms > 0) {   // workers from the device: make room and rebuild
+      cfg.num_workers = W = sms - sched_sms;
+      if (W < 1) return MPK_ERR_NOT_CORESIDENT;
+      g->bg = BuiltGraph{};
+      st = build_tgraph(cfg, &g->bg, &err);
+      if (st != MPK_OK) return st;
+    }
+  }
   static std::atomic<uint64_t> next_uid{1};
   g->uid = next_uid.fetch_add(1);
   g->num_sched_sms = sched_sms;
