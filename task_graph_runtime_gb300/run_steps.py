@@ -1,7 +1,7 @@
 """Run a few decode steps of a workload, for profiling.
 
   python -m task_graph_runtime_gb300.run_steps --workload qwen3_8b \
-      --mode mega --layers 1 --steps 3
+      --mode mega --layers 1 --steps 3 [--coarse]
 
 Seeded synthetic weights and KV cache are generated on cuda:0; `--layers`
 keeps only the first N decoder layers (a smaller case of the same kernels,
@@ -26,6 +26,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="keep the first N decoder layers (0: all)")
     ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--coarse", action="store_true",
+                    help="operator-level events (the coarse-grained graph)")
     args = ap.parse_args()
     wl = synth.WORKLOADS[args.workload]
     s = wl.shape
@@ -34,7 +36,8 @@ def main():
         wl = dataclasses.replace(wl, shape=s)
     W = synth.device_model_weights(s, 0, "cuda")
     g = mpk.Graph(s, wl.batch, page_size=wl.page_size,
-                  max_pages_per_seq=max(1, wl.max_pages_per_seq))
+                  max_pages_per_seq=max(1, wl.max_pages_per_seq),
+                  coarse_events=int(args.coarse))
     g.bind(mpk.Weights(W, s))
     g.set_mode({"mega": mpk.MODE_MEGAKERNEL, "kpo": mpk.MODE_KPO,
                 "kpo_graph": mpk.MODE_KPO_GRAPH}[args.mode])
@@ -58,7 +61,8 @@ def main():
     if g.status() != mpk.MPK_OK:
         raise RuntimeError(mpk.STATUS_NAMES[g.status()])
     g.close()
-    print(f"{args.workload} layers={s.n_layers} mode={args.mode}: "
+    print(f"{args.workload} layers={s.n_layers} mode={args.mode}"
+          f"{' coarse' if args.coarse else ''}: "
           f"{e0.elapsed_time(e1) / args.steps:.3f} ms/step, "
           f"{torch.cuda.memory_allocated() / 1e9:.2f} GB on the device")
 

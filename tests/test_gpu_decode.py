@@ -142,6 +142,19 @@ def test_tiny_tilings_match_oracle(tiny, workers, rows, chunks, sched):
     check_steps(gpu, ref)
 
 
+def test_tiny_coarse_events_match_oracle(tiny):
+    """Operator-level events (the coarse-grained graph of the Figure 4c
+    ablation: every task of an operator waits for all of the previous
+    operator) compute the same step, through the megakernel and the
+    kernel-per-operator build alike."""
+    wl, W, Wd, kv, tok = tiny
+    ref, _ = run_oracle(wl, W, kv, tok, steps=2)
+    for mode in (mpk.MODE_MEGAKERNEL, mpk.MODE_KPO):
+        gpu, _ = run_gpu(wl, Wd, kv, tok, steps=2, mode=mode, num_workers=5,
+                         coarse_events=1)
+        check_steps(gpu, ref)
+
+
 def test_tiny_batch_ragged_contexts():
     """Three sequences with contexts 0, 37 and 128 (an empty prior context,
     a ragged last page, full pages) and more chunks than tokens."""
