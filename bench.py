@@ -456,6 +456,7 @@ def run_ours(args, rank, world, local_rank):
         "same_run_modes": compare,
         "graph": {"tasks": ex["n_tasks"], "events": ex["n_events"],
                   "empty_tasks": ex["n_empty"], "workers": ex["n_workers"],
+                  "sched_sms": ex["n_sched_sms"],
                   "attn_chunks": ex["attn_chunks"]},
     }
     return out

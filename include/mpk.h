@@ -201,6 +201,8 @@ typedef struct {
   const int32_t* op_n_tasks;
   int64_t n_raw_events;        /* events before fusion                       */
   int64_t n_fused_events;      /* events after fusion, before normalisation  */
+  int n_sched_sms;             /* scheduler SMs of the launch (0: all-AOT)   */
+  int sched_warps_per_sm;
 } mpk_graph_export;
 
 /* Decompose one decode step of `shape` at `batch` sequences into per-tile

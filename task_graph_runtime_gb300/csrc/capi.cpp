@@ -280,6 +280,8 @@ mpk_status mpk_export_tgraph(const mpk_graph* g, mpk_graph_export* out) {
   out->op_n_tasks = g->op_n.data();
   out->n_raw_events = bg.n_raw;
   out->n_fused_events = bg.n_fused;
+  out->n_sched_sms = g->num_sched_sms;
+  out->sched_warps_per_sm = g->sched_warps_per_sm;
   return MPK_OK;
 }
 

@@ -94,7 +94,8 @@ class GraphExport(ctypes.Structure):
             "task_trig", "task_launch", "task_worker", "task_pre_id",
             "event_count", "event_first", "event_last", "op_kind",
             "op_layer", "op_n_tasks")] + [
-        ("n_raw_events", ctypes.c_int64), ("n_fused_events", ctypes.c_int64)]
+        ("n_raw_events", ctypes.c_int64), ("n_fused_events", ctypes.c_int64),
+        ("n_sched_sms", ctypes.c_int), ("sched_warps_per_sm", ctypes.c_int)]
 
 
 _lib = None
@@ -182,7 +183,8 @@ def mpk_export_tgraph(handle: int) -> Dict[str, np.ndarray]:
             np.zeros(0, np.int32)
     out = {k: getattr(ex, k) for k in ("n_tasks", "n_events", "n_ops",
                                         "n_empty", "n_workers", "attn_chunks",
-                                        "n_raw_events", "n_fused_events")}
+                                        "n_raw_events", "n_fused_events",
+                                        "n_sched_sms", "sched_warps_per_sm")}
     for k in ("task_kind", "task_op", "task_layer", "task_tile", "task_row0",
               "task_row1", "task_b", "task_g", "task_c", "task_dep",
               "task_trig", "task_launch", "task_worker", "task_pre_id"):

@@ -120,3 +120,26 @@ def test_cpp_builder_matches_oracle_builder(mpk_lib, case):
     assert [mpk.TASK_KINDS[k] for k in ex["op_kind"]] == \
         [o.kind for o in ref.ops]
     assert list(ex["op_n_tasks"]) == [o.n_tasks for o in ref.ops]
+
+
+@pytest.mark.parametrize("name,batch,kw,sched", [
+    ("tiny", 1, dict(num_workers=5), 0),              # every task AOT
+    ("chain_b8", 8, dict(num_workers=148), 0),        # no attention at all
+    ("qwen3_8b_b16", 16, dict(num_workers=148), 4),   # JIT attention
+    ("tiny", 1, dict(num_workers=5, num_sched_sms=2, sched_warps_per_sm=3), 2),
+])
+def test_scheduler_sms_follow_the_jit_tasks(mpk_lib, name, batch, kw, sched):
+    """Scheduler SMs default to 4 (Table 1) only when some task is JIT: a
+    graph whose tasks are all AOT never dispatches, and a count given
+    explicitly is kept."""
+    wl = synth.WORKLOADS[name]
+    g = mpk.Graph(wl.shape, batch, page_size=wl.page_size,
+                  max_pages_per_seq=max(1, wl.max_pages_per_seq), **kw)
+    ex = g.export()
+    has_jit = bool((ex["task_launch"] == 1).any())   # MPK_LAUNCH_JIT
+    assert ex["n_sched_sms"] == sched
+    assert ex["sched_warps_per_sm"] == kw.get("sched_warps_per_sm", 4)
+    if "num_sched_sms" not in kw:
+        assert (ex["n_sched_sms"] > 0) == has_jit
+    assert ex["n_workers"] == kw["num_workers"]
+    g.close()
