@@ -22,6 +22,9 @@ bool smem_layout(const BuiltGraph& bg, int pages_req, int limit,
   // bf16 x at batch 1; at batch > 1 one 2048-column segment of every
   // sequence plus a 512-column scratch row per sequence for the staging
   int xs = B == 1 ? round_up(kmax * 2, 16) : B * kPagePitch + B * 64 * 16;
+  // batch >= 8: the MatMul tile's 8 per-warp partial sums (fp32, up to 128
+  // rows of every sequence) are added through this buffer at the tile's end
+  if (B >= 8) xs = std::max(xs, 8 * B * 128 * 4);
   if (!chain) {
     const int grp = s.n_q_heads / s.n_kv_heads, d = s.head_dim;
     // query rows + 8 warp records (+ the new K/V rows)
